@@ -1,0 +1,279 @@
+/*
+ * libvbs: one step of batched beam search over a vocabulary, the KV-cache
+ * reorder that follows it, and the verify/accept step of blockwise parallel
+ * decoding, as a C ABI for one NVIDIA GB300 (sm_103a).
+ *
+ * Sources of the operations (cited by page title and section):
+ *   [BS] "Transformers中的Beam Search高效实现" (zhuanzhi.ai), section
+ *        多个样本同时进行beam search: the batched step, BeamHypotheses, padding,
+ *        the final choice.
+ *   [LM] "9.2 贪心搜索与束搜索：确定性与近似搜索" (llm_internals): §9.2.2 the four
+ *        sub-steps, the KV reorder paragraph and "何时结束"; §9.2.3 the length
+ *        penalty; §9.2.4 prompt sharing.
+ *   [BPD] "Blockwise Parallel Decoding for Deep Autoregressive Models"
+ *        (papercache notes): §3 predict / verify / accept; §4 the combined
+ *        scoring and proposal model.
+ *   [LS] "推荐一款超高速、多特性的高性能序列推理引擎—— LightSeq": "层级式解码计算"
+ *        names this path (vocabulary softmax, beam selection, cache refresh).
+ *
+ * Conventions for every call:
+ *   - Return value: VBS_OK (0) or a negative VBS_E* status; vbs_strerror()
+ *     names it.  Arguments are checked on the host before anything is
+ *     launched; a call that returns an error has launched nothing, except
+ *     VBS_ECUDA (the launch itself failed).
+ *   - Pointers marked "device" are CUDA device pointers owned by the caller.
+ *     The library reads and writes them only in work it enqueues on the
+ *     stream given to the call (or to the context's init); they must stay
+ *     valid until that work completes.  No call synchronises the stream unless
+ *     its comment says so.  No call after an init allocates device memory.
+ *   - Errors found on the device (bad input values, an exhausted block pool,
+ *     a wait that gave up) are recorded in a status word of the context and
+ *     reported by the *_status() calls; the kernels never trap.
+ *   - Logits are row-major with a row stride `ld` (elements) >= V; dtype is
+ *     VBS_F32 or VBS_BF16.  Logits must be finite or -inf, with at least one
+ *     finite value per row that is read.
+ */
+#ifndef VBS_H
+#define VBS_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* vbs_stream_t; /* the same type as cudaStream_t */
+
+enum {
+  VBS_OK = 0,
+  VBS_EINVAL = -1,   /* an argument is out of range or inconsistent */
+  VBS_ECUDA = -2,    /* a CUDA runtime call or kernel launch failed */
+  VBS_ENOMEM = -3,   /* device memory (init) or the paged block pool (step) ran out */
+  VBS_ESTATE = -4,   /* the call does not fit the context's state (e.g. more than max_len steps) */
+  VBS_EALIGN = -5,   /* a pointer or stride is not aligned as the call needs */
+  VBS_ETIMEOUT = -6, /* a bounded device-side wait gave up */
+  VBS_EINPUT = -7    /* the input data broke a precondition (NaN / +inf logits, ...) */
+};
+
+enum { VBS_F32 = 0, VBS_BF16 = 1 };
+/* length penalty ([LM] §9.2.3): GNMT ((5+|y|)/6)^alpha, or |y|^alpha */
+enum { VBS_LP_GNMT = 0, VBS_LP_POWER = 1 };
+/* early_stopping ([LM] §9.2.2 "何时结束"): False (heuristic), True (stop when W
+   hypotheses are finished), "never" (stop only when no live beam can overtake) */
+enum { VBS_ES_FALSE = 0, VBS_ES_TRUE = 1, VBS_ES_NEVER = 2 };
+
+/* Name of a status code (static string, never NULL). */
+const char* vbs_strerror(int status);
+/* Library version, major * 10000 + minor * 100 + patch. */
+int vbs_version(void);
+
+/* =============================================================================
+ * Batched beam search ([BS], [LM] §9.2.2-9.2.3)
+ * ============================================================================= */
+typedef struct vbs_bs vbs_bs;
+
+/*
+ * Create a beam-search context for `batch` sentences of W beams (R = batch*W
+ * rows) over a vocabulary of V tokens; allocate every workspace it will use
+ * (the streaming partials, the per-sentence finished sets, its own sequence
+ * buffer) so that steps never allocate.
+ *   eos            token that ends a hypothesis, or -1 for none
+ *   alpha          length-penalty exponent ([LM] §9.2.3; 0 = no normalisation)
+ *   early_stopping VBS_ES_*; lp_kind VBS_LP_*
+ *   max_len        maximum number of steps (generated tokens); sequences have
+ *                  max_len + 1 columns (BOS first)
+ *   bos, pad       the BOS token of column 0 and the PAD token of finished rows
+ *   dtype          VBS_F32 or VBS_BF16 logits
+ *   stream         the stream all of this context's work is enqueued on
+ * Limits: 1 <= W <= 16, V >= 2, batch >= 1, R*V < 2^31, 1 <= max_len.
+ * Errors: VBS_EINVAL, VBS_ENOMEM, VBS_ECUDA.  *ctx is NULL on error.
+ */
+int bs_init(vbs_bs** ctx, int batch, int W, int V, int eos, float alpha, int early_stopping, int lp_kind,
+            int max_len, int bos, int pad, int dtype, vbs_stream_t stream);
+
+/*
+ * Start a new decode ([BS]: beam_scores = 0 for beam 0 and -inf for the
+ * others, input_ids = BOS): writes scores[R] (device, fp32) and seqs[R,
+ * max_len+1] (device, int32, row-major; column 0 = BOS, the rest PAD), empties
+ * the finished sets, clears the done flags and the step counter.
+ * seqs may be NULL: the context then keeps the sequences in its own buffer
+ * (bs_seqs() returns it), and every later call must also pass NULL.
+ */
+int bs_reset(vbs_bs* ctx, float* scores, int32_t* seqs);
+
+/*
+ * One step for every sentence, in one kernel launch ([BS] loop body, [LM]
+ * §9.2.2): row log-softmax of logits[R, V] (row stride ld elements, device),
+ * add scores[r], rank each sentence's W*V candidates by (score desc, flat index
+ * j = w*V + v asc), walk the best 2W: an EOS hit within the top W joins the
+ * sentence's finished set with normalised score sum / lp(t) (t = this step's
+ * number), an EOS hit at rank >= W is skipped, any other candidate becomes a
+ * live beam until W are taken; then the sentence's stopping test runs once
+ * with the best candidate score.  A sentence already finished before this step
+ * emits score 0, token PAD and beam_idx -1 for its W rows.
+ * Outputs (device): scores[R] (in/out, the new cumulative scores),
+ *   beam_idx[R] (int32, the global parent row of each new row, -1 for a pad
+ *   row), tokens[R] (int32), seqs (in/out: parents' rows gathered, token
+ *   appended at column t; must be the buffer given to bs_reset), and, if
+ *   all_done is not NULL, *all_done = 1 when every sentence is finished.
+ * The logits are read once; a sentence already finished, and every row whose
+ * score is -inf, is not read at all.
+ * Errors: VBS_EINVAL (ld < V, NULL outputs), VBS_ESTATE (max_len steps already
+ *   run, or a seqs pointer other than the one given to bs_reset), VBS_EALIGN
+ *   never (unaligned logits take a slower element-wise path), VBS_ECUDA.
+ */
+int bs_step(vbs_bs* ctx, const void* logits, int64_t ld, float* scores, int32_t* seqs, int32_t* beam_idx,
+            int32_t* tokens, int32_t* all_done);
+
+/*
+ * Final choice ([BS] after the loop): the live beams of every sentence not yet
+ * finished are offered to its finished set with |y| = steps run; the winner is
+ * the highest normalised score, ties going to the entry latest in the set's
+ * insertion order.  out_seqs[batch, max_len+1] (device int32) gets BOS and the
+ * winner's tokens, then EOS when shorter than max_len+1 columns, then PAD;
+ * out_len[batch] the number of meaningful entries (EOS included);
+ * out_score[batch] the winner's normalised score.  scores/seqs are the
+ * buffers of the last bs_step (seqs NULL if the context keeps them).  The
+ * context is not changed: finalize may be called more than once.
+ */
+int bs_finalize(vbs_bs* ctx, const float* scores, const int32_t* seqs, int32_t* out_seqs, int32_t* out_len,
+                float* out_score);
+
+/*
+ * Copy the finished sets out (device buffers, for inspection):
+ * count[batch] int32; ns[batch*W] double normalised scores; len[batch*W] int32
+ * |y|; serial[batch*W] int32 insertion numbers (set order = ascending serial);
+ * tokens[batch*W, max_len+1] int32 (the first len entries are BOS + tokens);
+ * done[batch] int32.  Slots at or beyond count[b] are unused.  Any pointer may
+ * be NULL to skip that array.
+ */
+int bs_finished(vbs_bs* ctx, int32_t* count, double* ns, int32_t* len, int32_t* serial, int32_t* tokens,
+                int32_t* done);
+
+/* The context's own sequence buffer [R, max_len+1] (device), used when bs_reset got NULL. */
+int bs_seqs(vbs_bs* ctx, int32_t** seqs);
+/* Steps run since bs_reset. */
+int bs_steps(vbs_bs* ctx, int* steps);
+/* Synchronise the context's stream and return (then clear) its device status word. */
+int bs_status(vbs_bs* ctx);
+/* Free the context (synchronises its stream first). NULL is a no-op. */
+int bs_destroy(vbs_bs* ctx);
+
+/* =============================================================================
+ * KV-cache reorder ([LM] §9.2.2 KV paragraph; [LS] cache refresh)
+ * ============================================================================= */
+
+/* Geometry of a KV cache: layers L, KV heads H, head_dim D, positions t_max,
+   elem_bytes per number.  Naive layout [L][2][rows][H][t_max][D] (K then V). */
+typedef struct {
+  int layers;
+  int heads;
+  int head_dim;
+  int t_max;
+  int elem_bytes;
+} vbs_kv_desc;
+
+/*
+ * Naive reorder, out of place: for every row r with beam_idx[r] >= 0,
+ * dst[l][kv][r][h][0:t_valid][:] = src[l][kv][beam_idx[r]][h][0:t_valid][:];
+ * rows with beam_idx[r] = -1 are not written, positions >= t_valid neither.
+ * src and dst (device) must not overlap.  beam_idx[rows] int32 (device).
+ * Uses bulk (TMA) copies when head_dim * elem_bytes and both pointers are
+ * 16-byte aligned, element copies otherwise.
+ * Errors: VBS_EINVAL (t_valid > t_max, bad geometry, NULL), VBS_ECUDA.
+ */
+int kv_reorder(const vbs_kv_desc* desc, const void* src, void* dst, const int32_t* beam_idx, int rows,
+               int t_valid, vbs_stream_t stream);
+
+/*
+ * Paged cache with copy-on-write ([LM] §9.2.2: rewrite block-table entries,
+ * copy only when a shared block is written; §9.2.4 prompt sharing).
+ * The pool (device, caller-owned) is [num_blocks][L][2][H][block][D], with
+ * num_blocks = batch * blocks_per_sentence: sentence b owns blocks
+ * [b*S, (b+1)*S) (blocks are never shared across sentences).  The library
+ * owns the block table [R][max_blocks] int32 (row r's position p lives in pool
+ * block table[r][p / block] at slot p % block), the reference counts and the
+ * per-sentence free stacks.
+ */
+typedef struct vbs_pkv vbs_pkv;
+
+int kv_paged_init(vbs_pkv** pkv, const vbs_kv_desc* desc, int batch, int W, int blocks_per_sentence, int block,
+                  int max_blocks, void* pool, vbs_stream_t stream);
+/*
+ * The prompt: every sentence gets ceil(P / block) blocks that all W of its
+ * rows point at (one copy per sentence).  The caller then writes the prompt's
+ * K/V through the table of the sentence's first row and calls
+ * kv_paged_prepare(P) before the first generated position is written.
+ * Synchronises the stream (the tables are built on the host, once per decode).
+ */
+int kv_paged_prefill(vbs_pkv* pkv, int P);
+/*
+ * Make the block that position t_write lands in exclusive to every live row:
+ * a row whose table ends at that block boundary gets a fresh block; of the
+ * rows sharing a partly filled block the lowest keeps it and every other row
+ * gets a copy of its t_write % block filled slots (copy-on-write).
+ */
+int kv_paged_prepare(vbs_pkv* pkv, int t_write);
+/*
+ * Reorder by beam_idx[R] (device int32; -1 = pad row, left alone): table row r
+ * becomes row beam_idx[r]'s, counts are raised for the new references before
+ * the old ones are dropped, blocks reaching zero return to their sentence's
+ * stack, then kv_paged_prepare(t_valid) runs.  Two launches, no host sync.
+ * Errors: VBS_EINVAL (host checks); VBS_ENOMEM / VBS_EINVAL on the device are
+ * reported by kv_paged_status().
+ */
+int kv_paged_reorder(vbs_pkv* pkv, const int32_t* beam_idx, int t_valid);
+/* The device block table [R][max_blocks] and its row stride. */
+int kv_paged_table(vbs_pkv* pkv, const int32_t** table, int* max_blocks);
+/* Copy the reference counts [num_blocks] and per-row block counts [R] to device buffers (either may be NULL). */
+int kv_paged_counts(vbs_pkv* pkv, int32_t* refcnt, int32_t* nblk);
+/* Copy the block table [R][max_blocks] to a device buffer (entries at or beyond a row's block count are stale). */
+int kv_paged_copy_table(vbs_pkv* pkv, int32_t* out);
+/*
+ * Save / restore the allocator state (block table, block counts, reference
+ * counts, free stacks) into / from the context's own copy, device to device on
+ * the stream: a decode can restart from the state right after the prompt
+ * without a host round trip.  Pool contents are not copied; positions the
+ * restored tables do not cover are simply unused.
+ */
+int kv_paged_save(vbs_pkv* pkv);
+int kv_paged_restore(vbs_pkv* pkv);
+/* Synchronise the stream and return the number of filled slots copied by
+   copy-on-write since init (one slot = one position of one (layer, k/v, head)
+   run: head_dim * elem_bytes bytes read and the same written). */
+int kv_paged_cow_slots(vbs_pkv* pkv, int64_t* slots);
+/* Synchronise the stream and return (then clear) the device status word. */
+int kv_paged_status(vbs_pkv* pkv);
+int kv_paged_destroy(vbs_pkv* pkv);
+
+/* Synchronise `stream` and return (then clear) the status word of the calls
+   that have no context (kv_reorder's bounded waits). */
+int vbs_stateless_status(vbs_stream_t stream);
+
+/* =============================================================================
+ * Blockwise parallel decoding ([BPD] §3-§4)
+ * ============================================================================= */
+
+/*
+ * Predict: proposals[b, h] = argmax_v logits[b, h, v] for logits [B, k, V]
+ * (device, dense rows); argmax ties go to the lower token id.
+ */
+int bpd_propose(const void* logits, int B, int k, int V, int dtype, int32_t* proposals, vbs_stream_t stream);
+
+/*
+ * Verify + accept on the combined model's logits [B, k, k, V] (device, dense):
+ * logits[b, p, h, :] is head h+1 at proposal position p+1, i.e. given the
+ * prefix extended by proposals[b, 0..p].  khat[b] = 1 + the number of leading
+ * p = 0..k-2 with proposals[b, p+1] == argmax logits[b, p, 0, :]; if eos >= 0
+ * and an accepted proposal e < khat equals eos, khat = e + 1.
+ * next[b, h] = argmax logits[b, khat-1, h, :] (the next iteration's
+ * proposals).  Only the rows this needs are read.  1 <= k <= 32.
+ */
+int bpd_verify(const void* logits, const int32_t* proposals, int B, int k, int V, int dtype, int eos,
+               int32_t* khat, int32_t* next, vbs_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VBS_H */

@@ -1,0 +1,324 @@
+"""GB300-native batched beam-search step, KV-cache reorder and blockwise verify.
+
+A thin ctypes binding over ``libvbs.so`` (declared in ``include/vbs.h``): every
+function here only marshals torch tensors into pointers, sizes and the current
+CUDA stream; all of the work runs in the library's CUDA kernels.  There is no
+fallback: if the library is missing, every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = ["BeamSearch", "PagedKV", "kv_reorder", "bpd_propose", "bpd_verify", "VbsError", "lib",
+           "LP_GNMT", "LP_POWER", "ES_FALSE", "ES_TRUE", "ES_NEVER", "F32", "BF16"]
+
+F32, BF16 = 0, 1
+LP_GNMT, LP_POWER = 0, 1
+ES_FALSE, ES_TRUE, ES_NEVER = 0, 1, 2
+OK, EINVAL, ECUDA, ENOMEM, ESTATE, EALIGN, ETIMEOUT, EINPUT = 0, -1, -2, -3, -4, -5, -6, -7
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libvbs.so")
+
+_c_int, _c_i64, _c_f, _vp = ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
+_pp = ctypes.POINTER(ctypes.c_void_p)
+
+# name -> (restype, argtypes); mirrors include/vbs.h
+SIGNATURES = {
+    "vbs_strerror": (ctypes.c_char_p, [_c_int]),
+    "vbs_version": (_c_int, []),
+    "bs_init": (_c_int, [_pp, _c_int, _c_int, _c_int, _c_int, _c_f, _c_int, _c_int, _c_int, _c_int, _c_int,
+                         _c_int, _vp]),
+    "bs_reset": (_c_int, [_vp, _vp, _vp]),
+    "bs_step": (_c_int, [_vp, _vp, _c_i64, _vp, _vp, _vp, _vp, _vp]),
+    "bs_finalize": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp]),
+    "bs_finished": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "bs_seqs": (_c_int, [_vp, _pp]),
+    "bs_steps": (_c_int, [_vp, ctypes.POINTER(_c_int)]),
+    "bs_status": (_c_int, [_vp]),
+    "bs_destroy": (_c_int, [_vp]),
+    "kv_reorder": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _vp]),
+    "vbs_stateless_status": (_c_int, [_vp]),
+    "kv_paged_init": (_c_int, [_pp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp]),
+    "kv_paged_prefill": (_c_int, [_vp, _c_int]),
+    "kv_paged_prepare": (_c_int, [_vp, _c_int]),
+    "kv_paged_reorder": (_c_int, [_vp, _vp, _c_int]),
+    "kv_paged_table": (_c_int, [_vp, _pp, ctypes.POINTER(_c_int)]),
+    "kv_paged_counts": (_c_int, [_vp, _vp, _vp]),
+    "kv_paged_copy_table": (_c_int, [_vp, _vp]),
+    "kv_paged_save": (_c_int, [_vp]),
+    "kv_paged_cow_slots": (_c_int, [_vp, ctypes.POINTER(_c_i64)]),
+    "kv_paged_restore": (_c_int, [_vp]),
+    "kv_paged_status": (_c_int, [_vp]),
+    "kv_paged_destroy": (_c_int, [_vp]),
+    "bpd_propose": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _vp, _vp]),
+    "bpd_verify": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _vp]),
+}
+
+_LIB = None
+
+
+class VbsError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        msg = lib().vbs_strerror(status).decode() if _LIB is not None else str(status)
+        super().__init__(f"{what}: {msg} ({status})" if what else f"{msg} ({status})")
+        self.status = status
+
+
+def lib():
+    """Load libvbs.so (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -m verify_bs_step_gb300._build`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype, fn.argtypes = res, args
+        _LIB = L
+    return _LIB
+
+
+def _check(st: int, what: str):
+    if st != OK:
+        raise VbsError(st, what)
+
+
+def _dev_ptr(t: torch.Tensor, name: str, dtype=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return _vp(t.data_ptr())
+
+
+def _stream(device=None):
+    return _vp(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _dtype_code(dt) -> int:
+    if dt == torch.bfloat16:
+        return BF16
+    if dt == torch.float32:
+        return F32
+    raise ValueError(f"logits dtype must be bfloat16 or float32, got {dt}")
+
+
+class BeamSearch:
+    """Batched beam search over `batch` sentences x W beams (libvbs bs_*).
+
+    Holds the decode's device buffers (scores [R] fp32, seqs [R, max_len+1]
+    int32, beam_idx [R], tokens [R], an all-done flag) so steps allocate nothing.
+    All work goes on the stream that is current at construction.
+    """
+
+    def __init__(self, batch: int, W: int, V: int, *, eos: int = -1, alpha: float = 1.0,
+                 early_stopping: int = ES_FALSE, lp_kind: int = LP_GNMT, max_len: int = 64, bos: int = 0,
+                 pad: int = -1, dtype=torch.bfloat16, device="cuda"):
+        self.batch, self.W, self.V, self.max_len = batch, W, V, max_len
+        self.R = batch * W
+        self.device = torch.device(device)
+        self.dtype = dtype
+        self._stream_obj = torch.cuda.current_stream(self.device)
+        self.stream = _vp(self._stream_obj.cuda_stream)
+        ctx = _vp()
+        _check(lib().bs_init(ctypes.byref(ctx), batch, W, V, eos, alpha, early_stopping, lp_kind, max_len, bos,
+                             pad, _dtype_code(dtype), self.stream), "bs_init")
+        self.ctx = ctx
+        dev = self.device
+        self.scores = torch.empty(self.R, dtype=torch.float32, device=dev)
+        self.seqs = torch.empty(self.R, max_len + 1, dtype=torch.int32, device=dev)
+        self.beam_idx = torch.empty(self.R, dtype=torch.int32, device=dev)
+        self.tokens = torch.empty(self.R, dtype=torch.int32, device=dev)
+        self.all_done = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.reset()
+
+    def reset(self):
+        _check(lib().bs_reset(self.ctx, _vp(self.scores.data_ptr()), _vp(self.seqs.data_ptr())), "bs_reset")
+
+    def step(self, logits: torch.Tensor):
+        """One step on logits [R, V] (unit stride along V); returns (beam_idx, tokens, scores) views."""
+        if logits.dim() != 2 or logits.shape[0] != self.R or logits.shape[1] != self.V or logits.stride(1) != 1:
+            raise ValueError(f"logits must be [{self.R}, {self.V}] with unit stride along V")
+        if logits.dtype != self.dtype:
+            raise ValueError(f"logits must be {self.dtype}")
+        _check(lib().bs_step(self.ctx, _dev_ptr(logits, "logits"), logits.stride(0), _vp(self.scores.data_ptr()),
+                             _vp(self.seqs.data_ptr()), _vp(self.beam_idx.data_ptr()),
+                             _vp(self.tokens.data_ptr()), _vp(self.all_done.data_ptr())), "bs_step")
+        return self.beam_idx, self.tokens, self.scores
+
+    def finalize(self):
+        """(out_seqs [batch, max_len+1] int32, out_len [batch] int32, out_score [batch] fp32)."""
+        out = torch.empty(self.batch, self.max_len + 1, dtype=torch.int32, device=self.device)
+        out_len = torch.empty(self.batch, dtype=torch.int32, device=self.device)
+        out_score = torch.empty(self.batch, dtype=torch.float32, device=self.device)
+        _check(lib().bs_finalize(self.ctx, _vp(self.scores.data_ptr()), _vp(self.seqs.data_ptr()),
+                                 _vp(out.data_ptr()), _vp(out_len.data_ptr()), _vp(out_score.data_ptr())),
+               "bs_finalize")
+        return out, out_len, out_score
+
+    def finished(self):
+        """The finished sets: dict of count [B], ns [R] fp64, len [R], serial [R], tokens [R, max_len+1], done [B]."""
+        d = self.device
+        f = {"count": torch.empty(self.batch, dtype=torch.int32, device=d),
+             "ns": torch.empty(self.R, dtype=torch.float64, device=d),
+             "len": torch.empty(self.R, dtype=torch.int32, device=d),
+             "serial": torch.empty(self.R, dtype=torch.int32, device=d),
+             "tokens": torch.empty(self.R, self.max_len + 1, dtype=torch.int32, device=d),
+             "done": torch.empty(self.batch, dtype=torch.int32, device=d)}
+        _check(lib().bs_finished(self.ctx, *[_vp(f[k].data_ptr()) for k in
+                                             ("count", "ns", "len", "serial", "tokens", "done")]), "bs_finished")
+        return f
+
+    def steps(self) -> int:
+        n = _c_int()
+        _check(lib().bs_steps(self.ctx, ctypes.byref(n)), "bs_steps")
+        return n.value
+
+    def status(self) -> int:
+        """Synchronise and return the device status word (0 = OK)."""
+        return lib().bs_status(self.ctx)
+
+    def close(self):
+        if getattr(self, "ctx", None) is not None and self.ctx.value:
+            lib().bs_destroy(self.ctx)
+            self.ctx = _vp()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class _KvDesc(ctypes.Structure):
+    _fields_ = [("layers", _c_int), ("heads", _c_int), ("head_dim", _c_int), ("t_max", _c_int),
+                ("elem_bytes", _c_int)]
+
+
+def kv_reorder(src: torch.Tensor, dst: torch.Tensor, beam_idx: torch.Tensor, t_valid: int):
+    """dst[:, :, r, :, :t_valid] = src[:, :, beam_idx[r], :, :t_valid] for beam_idx[r] >= 0.
+
+    src, dst: contiguous [L, 2, rows, H, T_max, D] CUDA tensors; beam_idx: int32 [rows].
+    """
+    if src.shape != dst.shape or src.dim() != 6 or src.shape[1] != 2:
+        raise ValueError("src and dst must be [L, 2, rows, H, T_max, D]")
+    if not (src.is_contiguous() and dst.is_contiguous()):
+        raise ValueError("src and dst must be contiguous")
+    L, _, rows, H, T, D = src.shape
+    desc = _KvDesc(L, H, D, T, src.element_size())
+    _check(lib().kv_reorder(ctypes.byref(desc), _dev_ptr(src, "src"), _dev_ptr(dst, "dst"),
+                            _dev_ptr(beam_idx, "beam_idx", torch.int32), rows, t_valid, _stream(src.device)),
+           "kv_reorder")
+
+
+class PagedKV:
+    """Paged KV cache with copy-on-write (libvbs kv_paged_*).
+
+    The pool is a [batch * blocks_per_sentence, L, 2, H, block, D] tensor; the
+    library owns the block table, the reference counts and the free stacks.
+    """
+
+    def __init__(self, batch: int, W: int, L: int, H: int, D: int, *, blocks_per_sentence: int,
+                 max_blocks: int, block: int = 16, dtype=torch.bfloat16, device="cuda", pool=None):
+        self.batch, self.W, self.R = batch, W, batch * W
+        self.L, self.H, self.D, self.block = L, H, D, block
+        self.S, self.max_blocks = blocks_per_sentence, max_blocks
+        self.device = torch.device(device)
+        if pool is None:
+            pool = torch.zeros(batch * blocks_per_sentence, L, 2, H, block, D, dtype=dtype, device=self.device)
+        self.pool = pool
+        self.stream = _vp(torch.cuda.current_stream(self.device).cuda_stream)
+        desc = _KvDesc(L, H, D, max_blocks * block, pool.element_size())
+        ctx = _vp()
+        _check(lib().kv_paged_init(ctypes.byref(ctx), ctypes.byref(desc), batch, W, blocks_per_sentence, block,
+                                   max_blocks, _dev_ptr(pool, "pool"), self.stream), "kv_paged_init")
+        self.ctx = ctx
+        ptr = _vp()
+        mb = _c_int()
+        _check(lib().kv_paged_table(self.ctx, ctypes.byref(ptr), ctypes.byref(mb)), "kv_paged_table")
+        self._table_ptr = ptr.value
+
+    def prefill(self, P: int):
+        _check(lib().kv_paged_prefill(self.ctx, P), "kv_paged_prefill")
+
+    def prepare(self, t_write: int):
+        _check(lib().kv_paged_prepare(self.ctx, t_write), "kv_paged_prepare")
+
+    def reorder(self, beam_idx: torch.Tensor, t_valid: int):
+        _check(lib().kv_paged_reorder(self.ctx, _dev_ptr(beam_idx, "beam_idx", torch.int32), t_valid),
+               "kv_paged_reorder")
+
+    def save(self):
+        """Snapshot the allocator state on the device (no host round trip)."""
+        _check(lib().kv_paged_save(self.ctx), "kv_paged_save")
+
+    def restore(self):
+        """Return the allocator to the last snapshot (no host round trip)."""
+        _check(lib().kv_paged_restore(self.ctx), "kv_paged_restore")
+
+    def table(self) -> torch.Tensor:
+        """A copy of the block table [R, max_blocks] (int32, on the device)."""
+        out = torch.empty(self.R, self.max_blocks, dtype=torch.int32, device=self.device)
+        _check(lib().kv_paged_copy_table(self.ctx, _vp(out.data_ptr())), "kv_paged_copy_table")
+        return out
+
+    def counts(self):
+        """(refcnt [batch * blocks_per_sentence], nblk [R]) as int32 device tensors."""
+        rc = torch.empty(self.batch * self.S, dtype=torch.int32, device=self.device)
+        nb = torch.empty(self.R, dtype=torch.int32, device=self.device)
+        _check(lib().kv_paged_counts(self.ctx, _vp(rc.data_ptr()), _vp(nb.data_ptr())), "kv_paged_counts")
+        return rc, nb
+
+    def cow_slots(self) -> int:
+        """Filled slots copied by copy-on-write since init (synchronises)."""
+        n = _c_i64()
+        _check(lib().kv_paged_cow_slots(self.ctx, ctypes.byref(n)), "kv_paged_cow_slots")
+        return n.value
+
+    def status(self) -> int:
+        return lib().kv_paged_status(self.ctx)
+
+    def close(self):
+        if getattr(self, "ctx", None) is not None and self.ctx.value:
+            lib().kv_paged_destroy(self.ctx)
+            self.ctx = _vp()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def bpd_propose(logits: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+    """Predict: argmax over V of logits [B, k, V] (dense) -> int32 [B, k]."""
+    if logits.dim() != 3 or not logits.is_contiguous():
+        raise ValueError("logits must be a contiguous [B, k, V] tensor")
+    B, k, V = logits.shape
+    if out is None:
+        out = torch.empty(B, k, dtype=torch.int32, device=logits.device)
+    _check(lib().bpd_propose(_dev_ptr(logits, "logits"), B, k, V, _dtype_code(logits.dtype),
+                             _dev_ptr(out, "out", torch.int32), _stream(logits.device)), "bpd_propose")
+    return out
+
+
+def bpd_verify(logits: torch.Tensor, proposals: torch.Tensor, eos: int = -1, khat: torch.Tensor | None = None,
+               next_out: torch.Tensor | None = None):
+    """Verify + accept on combined logits [B, k, k, V] -> (khat int32 [B], next proposals int32 [B, k])."""
+    if logits.dim() != 4 or logits.shape[1] != logits.shape[2] or not logits.is_contiguous():
+        raise ValueError("logits must be a contiguous [B, k, k, V] tensor")
+    B, k, _, V = logits.shape
+    if proposals.shape != (B, k) or not proposals.is_contiguous():
+        raise ValueError("proposals must be a contiguous [B, k] int32 tensor")
+    if khat is None:
+        khat = torch.empty(B, dtype=torch.int32, device=logits.device)
+    if next_out is None:
+        next_out = torch.empty(B, k, dtype=torch.int32, device=logits.device)
+    _check(lib().bpd_verify(_dev_ptr(logits, "logits"), _dev_ptr(proposals, "proposals", torch.int32), B, k, V,
+                            _dtype_code(logits.dtype), eos, _dev_ptr(khat, "khat", torch.int32),
+                            _dev_ptr(next_out, "next", torch.int32), _stream(logits.device)), "bpd_verify")
+    return khat, next_out

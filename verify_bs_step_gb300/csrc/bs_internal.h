@@ -1,0 +1,91 @@
+// Internal interface between the C-ABI layer and the beam-step kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace vbs {
+
+constexpr int WMAX = 16;          // beams per sentence
+constexpr int KMAX = 2 * WMAX;    // candidates kept per row (2W)
+constexpr int PART_KEYS = 512;    // keys one row merge can hold (partials x K)
+
+struct BsArgs {
+  const void* logits;
+  int64_t ld;
+  int dtype;
+  int B, W, V, K, R;
+  int64_t per;                    // elements of the flattened [R, V] space per CTA
+  int P;                          // partial slots per row
+  float* scores;
+  int32_t* seqs;
+  int seq_ld;                     // max_len + 1
+  int32_t* beam_idx;
+  int32_t* tokens;
+  int32_t* all_done_out;          // optional, caller's
+  int32_t* all_done_dev;          // the context's own flag
+  int t;                          // 1-based step number
+  int eos, bos, pad, early_stopping, lp_kind, max_len;
+  double alpha;
+  // workspace
+  float* part_M;
+  float* part_l;
+  unsigned long long* part_key;
+  double* row_lse;
+  unsigned long long* row_key;
+  int* row_ticket;
+  int* sent_ticket;
+  int* glob_ticket;
+  int* done;
+  // finished sets
+  double* fin_ns;
+  int* fin_len;
+  int* fin_serial;
+  int32_t* fin_tok;
+  int* fin_count;
+  int* fin_next;
+  double* fin_worst;
+  int* status;
+};
+
+int launch_bs_step(const BsArgs& a, int grid, bool vector_ok, cudaStream_t s);
+int launch_bs_reset(const BsArgs& a, cudaStream_t s);
+int launch_bs_finalize(const BsArgs& a, const float* scores, const int32_t* seqs, int32_t* out_seqs,
+                       int32_t* out_len, float* out_score, cudaStream_t s);
+int bs_threads_per_cta();
+
+// KV reorder
+struct KvGeom {
+  int L, H, rows;
+  int64_t seg_stride;             // bytes between consecutive (l, kv, r, h) segments
+  int64_t copy_bytes;             // bytes copied per segment
+};
+int launch_kv_naive(const KvGeom& g, const void* src, void* dst, const int32_t* beam_idx, bool bulk_ok,
+                    int elem_bytes, int* status, int num_sms, cudaStream_t s);
+
+struct PagedArgs {
+  int B, W, S, MB, block, L, H;
+  int64_t block_bytes;            // bytes of one pool block
+  int64_t slot_bytes;             // bytes of one position within one (l, kv, h) run
+  char* pool;
+  int32_t* table;                 // [R, MB]
+  int32_t* nblk;                  // [R]
+  int32_t* refcnt;                // [B*S]
+  int32_t* stack;                 // [B*S]
+  int32_t* top;                   // [B]
+  int4* tasks;                    // [R] (src block, dst block, filled slots, -)
+  int32_t* task_count;
+  int32_t* cow_ticket;
+  unsigned long long* cow_slots;  // filled slots copied, summed (x L*2*H runs)
+  int* status;
+};
+int launch_kv_paged_remap(const PagedArgs& a, const int32_t* beam_idx, int t_valid, cudaStream_t s);
+int launch_kv_paged_cow(const PagedArgs& a, bool bulk_ok, int num_sms, cudaStream_t s);
+
+// blockwise parallel decoding
+int launch_bpd_propose(const void* logits, int B, int k, int V, int dtype, bool vec_ok, int32_t* proposals,
+                       cudaStream_t s);
+int launch_bpd_verify(const void* logits, const int32_t* proposals, int B, int k, int V, int dtype, bool vec_ok,
+                      int eos, int32_t* khat, int32_t* next, cudaStream_t s);
+
+}  // namespace vbs

@@ -1,0 +1,378 @@
+// KV-cache reorder by beam_idx (sm_103a): naive gather and paged block table
+// with copy-on-write.
+//
+// What is computed follows "9.2 贪心搜索与束搜索：确定性与近似搜索" §9.2.2 (the
+// cache paragraph: row r continues from the cache of its parent beam_idx[r]; the
+// naive way gathers every layer's K and V; a paged cache rewrites block-table
+// entries and copies only when a shared block is written) and §9.2.4 (prompt
+// sharing).
+//
+// Both copy paths are pure byte movement, so they run on the bulk-copy (TMA)
+// engine: one elected thread per CTA keeps a ring of shared-memory stages full
+// with cp.async.bulk global->shared loads (completing on mbarriers) and drains
+// them with cp.async.bulk shared->global stores (bulk groups).  The remap of
+// the paged table is sentence-local (blocks are never shared across
+// sentences), so it runs one CTA per sentence on shared-memory copies of the
+// sentence's table rows, reference counts and free stack, with no global
+// atomics and a deterministic allocation order.
+
+#include "common.cuh"
+#include "bs_internal.h"
+
+namespace vbs {
+
+constexpr int KV_STAGES = 6;
+constexpr int KV_CHUNK = 16384;       // bytes per bulk copy
+constexpr int KV_CTAS_PER_SM = 2;
+
+// ---------------------------------------------------------------------------------------
+// the bulk-copy engine: items i = blockIdx.x, blockIdx.x + gridDim.x, ...;
+// Map(i, &src, &dst, &bytes) returns false (or bytes == 0) for an item with nothing to copy.
+// ---------------------------------------------------------------------------------------
+
+template <class Map>
+__device__ void bulk_copy_items(const Map& map, int64_t n_items, int* status) {
+  extern __shared__ __align__(128) unsigned char kv_smem[];
+  __shared__ __align__(8) u64 bars[KV_STAGES];
+  if (threadIdx.x != 0) return;
+  for (int s = 0; s < KV_STAGES; ++s) mbar_init(&bars[s], 1);
+  fence_mbar_init();
+
+  const int64_t first = blockIdx.x, step = gridDim.x;
+  const int64_t n_mine = first < n_items ? (n_items - first + step - 1) / step : 0;
+  auto issue_load = [&](int64_t k) {
+    const int st = static_cast<int>(k % KV_STAGES);
+    const char* src = nullptr;
+    char* dst = nullptr;
+    u32 bytes = 0;
+    map(first + k * step, src, dst, bytes);
+    mbar_expect_tx(&bars[st], bytes);
+    if (bytes) bulk_g2s(kv_smem + st * KV_CHUNK, src, bytes, &bars[st]);
+  };
+  for (int64_t k = 0; k < KV_STAGES - 1 && k < n_mine; ++k) issue_load(k);
+  bool ok = true;
+  for (int64_t k = 0; k < n_mine; ++k) {
+    const int st = static_cast<int>(k % KV_STAGES);
+    if (ok && !mbar_wait(&bars[st], static_cast<u32>((k / KV_STAGES) & 1))) {
+      set_status(status, VBS_ETIMEOUT);
+      ok = false;
+    }
+    const char* src = nullptr;
+    char* dst = nullptr;
+    u32 bytes = 0;
+    map(first + k * step, src, dst, bytes);
+    if (ok && bytes) bulk_s2g(dst, kv_smem + st * KV_CHUNK, bytes);
+    bulk_commit();
+    if (k + KV_STAGES - 1 < n_mine) {
+      bulk_wait_read<1>();                 // the stage of item k-1 is free again
+      if (ok) issue_load(k + KV_STAGES - 1);
+    }
+  }
+  bulk_wait<0>();
+  if (!ok) {
+    // give loads still in flight a bounded chance to land before the CTA exits
+    for (int s = 0; s < KV_STAGES; ++s) mbar_wait(&bars[s], 0, 1u << 16);
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+// naive gather: dst[l, kv, r, h, 0:t] = src[l, kv, beam_idx[r], h, 0:t]
+// ---------------------------------------------------------------------------------------
+
+struct NaiveMap {
+  const char* src;
+  char* dst;
+  const int32_t* bi;
+  int H, rows;
+  int64_t seg_stride, copy_bytes, nch;
+  __device__ void operator()(int64_t item, const char*& s, char*& d, u32& bytes) const {
+    const int64_t c = item % nch;
+    const int64_t seg = item / nch;
+    const int h = static_cast<int>(seg % H);
+    const int r = static_cast<int>((seg / H) % rows);
+    const int64_t lkv = seg / (static_cast<int64_t>(H) * rows);
+    const int p = __ldg(bi + r);
+    bytes = 0;
+    if (p < 0) return;
+    const int64_t off = c * KV_CHUNK;
+    const int64_t rem = copy_bytes - off;
+    bytes = static_cast<u32>(rem < KV_CHUNK ? rem : KV_CHUNK);
+    s = src + ((lkv * rows + p) * H + h) * seg_stride + off;
+    d = dst + ((lkv * rows + r) * H + h) * seg_stride + off;
+  }
+};
+
+__global__ void __launch_bounds__(32) kv_naive_bulk_kernel(NaiveMap map, int64_t n_items, int* status) {
+  bulk_copy_items(map, n_items, status);
+}
+
+// Element-wise fallback for layouts the bulk engine cannot take (alignment).
+template <typename W>
+__global__ void kv_naive_plain_kernel(const char* src, char* dst, const int32_t* bi, int H, int rows,
+                                      int64_t seg_stride, int64_t copy_words, int64_t n_segs) {
+  const int64_t total = n_segs * copy_words;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t seg = i / copy_words, w = i % copy_words;
+    const int h = static_cast<int>(seg % H);
+    const int r = static_cast<int>((seg / H) % rows);
+    const int64_t lkv = seg / (static_cast<int64_t>(H) * rows);
+    const int p = __ldg(bi + r);
+    if (p < 0) continue;
+    const W* s = reinterpret_cast<const W*>(src + ((lkv * rows + p) * H + h) * seg_stride);
+    W* d = reinterpret_cast<W*>(dst + ((lkv * rows + r) * H + h) * seg_stride);
+    d[w] = s[w];
+  }
+}
+
+int launch_kv_naive(const KvGeom& g, const void* src, void* dst, const int32_t* beam_idx, bool bulk_ok,
+                    int elem_bytes, int* status, int num_sms, cudaStream_t s) {
+  const int64_t n_segs = static_cast<int64_t>(g.L) * 2 * g.rows * g.H;
+  if (g.copy_bytes == 0 || n_segs == 0) return VBS_OK;
+  if (bulk_ok) {
+    NaiveMap m{static_cast<const char*>(src), static_cast<char*>(dst), beam_idx, g.H, g.rows,
+               g.seg_stride, g.copy_bytes, (g.copy_bytes + KV_CHUNK - 1) / KV_CHUNK};
+    const int64_t n_items = n_segs * m.nch;
+    const size_t smem = static_cast<size_t>(KV_STAGES) * KV_CHUNK;
+    static bool attr_set = false;
+    if (!attr_set) {
+      cudaFuncSetAttribute(kv_naive_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem));
+      attr_set = true;
+    }
+    const int grid = static_cast<int>(std::min<int64_t>(n_items, static_cast<int64_t>(num_sms) * KV_CTAS_PER_SM));
+    kv_naive_bulk_kernel<<<grid, 32, smem, s>>>(m, n_items, status);
+  } else {
+    const int64_t grid = std::min<int64_t>(static_cast<int64_t>(num_sms) * 8, 1 << 16);
+    const char* sp = static_cast<const char*>(src);
+    char* dp = static_cast<char*>(dst);
+    if (g.copy_bytes % 4 == 0 && g.seg_stride % 4 == 0 && elem_bytes % 4 == 0)
+      kv_naive_plain_kernel<uint32_t><<<static_cast<int>(grid), 256, 0, s>>>(
+          sp, dp, beam_idx, g.H, g.rows, g.seg_stride, g.copy_bytes / 4, n_segs);
+    else if (g.copy_bytes % 2 == 0 && g.seg_stride % 2 == 0)
+      kv_naive_plain_kernel<uint16_t><<<static_cast<int>(grid), 256, 0, s>>>(
+          sp, dp, beam_idx, g.H, g.rows, g.seg_stride, g.copy_bytes / 2, n_segs);
+    else
+      kv_naive_plain_kernel<uint8_t><<<static_cast<int>(grid), 256, 0, s>>>(
+          sp, dp, beam_idx, g.H, g.rows, g.seg_stride, g.copy_bytes, n_segs);
+  }
+  return cudaGetLastError() == cudaSuccess ? VBS_OK : VBS_ECUDA;
+}
+
+// ---------------------------------------------------------------------------------------
+// paged: remap + reference counts + free stack + copy-on-write tasks (one CTA per sentence)
+// ---------------------------------------------------------------------------------------
+
+constexpr int REMAP_NT = 256;
+
+__global__ void __launch_bounds__(REMAP_NT) kv_paged_remap_kernel(const PagedArgs a, const int32_t* bi,
+                                                                  int t_valid) {
+  extern __shared__ int32_t rs[];
+  const int b = blockIdx.x, W = a.W, S = a.S, MB = a.MB;
+  const int r0 = b * W;
+  int32_t* old = rs;                   // [W][MB]
+  int32_t* rc = old + W * MB;          // [S] counts now
+  int32_t* rc0 = rc + S;               // [S] counts before
+  int32_t* stk = rc0 + S;              // [S]
+  __shared__ int nold[WMAX], par[WMAX], nnew[WMAX], tail[WMAX];
+  __shared__ int top, any_live;
+  const int tid = threadIdx.x;
+
+  if (tid == 0) any_live = 0;
+  __syncthreads();
+  if (tid < W) {
+    nold[tid] = a.nblk[r0 + tid];
+    par[tid] = __ldg(bi + r0 + tid);
+    if (par[tid] >= 0) {
+      if (par[tid] < r0 || par[tid] >= r0 + W) set_status(a.status, VBS_EINVAL);
+      atomicOr(&any_live, 1);
+    }
+  }
+  __syncthreads();
+  if (!any_live) {
+    if (tid == 0) {
+      // a finished sentence: nothing moves, nothing is copied
+    }
+    return;
+  }
+  for (int i = tid; i < W * MB; i += REMAP_NT) old[i] = a.table[static_cast<int64_t>(r0) * MB + i];
+  for (int j = tid; j < S; j += REMAP_NT) {
+    rc[j] = a.refcnt[static_cast<int64_t>(b) * S + j];
+    rc0[j] = rc[j];
+    stk[j] = a.stack[static_cast<int64_t>(b) * S + j];
+  }
+  if (tid == 0) top = a.top[b];
+  if (tid < W && (par[tid] < r0 || par[tid] >= r0 + W)) par[tid] = -1;
+  __syncthreads();
+
+  // new references first, then drop the old ones: a block shared by parent and
+  // child never reaches zero in between
+  for (int i = tid; i < W * MB; i += REMAP_NT) {
+    const int w = i / MB, s = i - w * MB;
+    const int p = par[w];
+    if (p >= 0 && s < nold[p - r0]) {
+      const int blk = old[(p - r0) * MB + s] - b * S;
+      if (blk >= 0 && blk < S) atomicAdd(&rc[blk], 1);
+      else set_status(a.status, VBS_EINVAL);
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < W * MB; i += REMAP_NT) {
+    const int w = i / MB, s = i - w * MB;
+    if (par[w] >= 0 && s < nold[w]) {
+      const int blk = old[w * MB + s] - b * S;
+      if (blk >= 0 && blk < S) atomicSub(&rc[blk], 1);
+    }
+  }
+  __syncthreads();
+  // freed blocks go back on the stack in ascending id order
+  if (tid < 32) {
+    for (int j0 = 0; j0 < S; j0 += 32) {
+      const int j = j0 + tid;
+      const bool freed = j < S && rc0[j] > 0 && rc[j] == 0;
+      const u32 m = __ballot_sync(FULL, freed);
+      const int pos = top + __popc(m & ((1u << tid) - 1u));
+      if (freed && pos < S) stk[pos] = b * S + j;
+      __syncwarp();
+      if (tid == 0) top = min(S, top + __popc(m));
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+
+  // make the block holding position t_valid exclusive to each live row
+  if (tid == 0) {
+    const int i = t_valid / a.block, fill = t_valid % a.block;
+    int kept[WMAX];
+    int n_kept = 0;
+    for (int w = 0; w < W; ++w) {
+      tail[w] = -1;
+      const int p = par[w];
+      if (p < 0) { nnew[w] = nold[w]; continue; }
+      const int n = nold[p - r0];
+      nnew[w] = n;
+      if (n == i) {                                       // a fresh block, nothing to copy
+        if (top == 0) { set_status(a.status, VBS_ENOMEM); continue; }
+        const int nb = stk[--top];
+        rc[nb - b * S] = 1;
+        tail[w] = nb;
+        nnew[w] = i + 1;
+      } else if (n == i + 1) {
+        const int blk = old[(p - r0) * MB + i];
+        if (rc[blk - b * S] == 1) continue;
+        bool is_kept = false;
+        for (int q = 0; q < n_kept; ++q) is_kept |= kept[q] == blk;
+        if (!is_kept) { kept[n_kept++] = blk; continue; }  // the lowest row keeps the shared block
+        if (top == 0) { set_status(a.status, VBS_ENOMEM); continue; }
+        const int nb = stk[--top];
+        rc[nb - b * S] = 1;
+        rc[blk - b * S] -= 1;
+        tail[w] = nb;
+        const int slot = atomicAdd(a.task_count, 1);
+        a.tasks[slot] = make_int4(blk, nb, fill, 0);
+        atomicAdd(a.cow_slots, static_cast<unsigned long long>(fill) * (a.L * 2 * a.H));
+      } else {
+        set_status(a.status, VBS_EINVAL);                 // the table does not match t_valid
+      }
+    }
+  }
+  __syncthreads();
+
+  // write back
+  const int ti = t_valid / a.block;
+  for (int i = tid; i < W * MB; i += REMAP_NT) {
+    const int w = i / MB, s = i - w * MB;
+    const int p = par[w];
+    if (p < 0) continue;
+    int v = s < nold[p - r0] ? old[(p - r0) * MB + s] : -1;
+    if (s == ti && tail[w] >= 0) v = tail[w];
+    if (s < nnew[w]) a.table[static_cast<int64_t>(r0 + w) * MB + s] = v;
+  }
+  if (tid < W) a.nblk[r0 + tid] = nnew[tid];
+  for (int j = tid; j < S; j += REMAP_NT) {
+    a.refcnt[static_cast<int64_t>(b) * S + j] = rc[j];
+    a.stack[static_cast<int64_t>(b) * S + j] = stk[j];
+  }
+  if (tid == 0) a.top[b] = top;
+}
+
+int launch_kv_paged_remap(const PagedArgs& a, const int32_t* beam_idx, int t_valid, cudaStream_t s) {
+  const size_t smem = (static_cast<size_t>(a.W) * a.MB + 3 * static_cast<size_t>(a.S)) * sizeof(int32_t);
+  if (smem > 200 * 1024) return VBS_EINVAL;
+  static size_t attr = 0;
+  if (smem > 48 * 1024 && smem > attr) {
+    cudaFuncSetAttribute(kv_paged_remap_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    attr = smem;
+  }
+  kv_paged_remap_kernel<<<a.B, REMAP_NT, smem, s>>>(a, beam_idx, t_valid);
+  return cudaGetLastError() == cudaSuccess ? VBS_OK : VBS_ECUDA;
+}
+
+// copy-on-write: task q copies the filled slots of every (l, kv, h) run of a block
+struct CowMap {
+  const char* pool;
+  const int4* tasks;
+  int n_runs;                       // L * 2 * H
+  int64_t block_bytes, run_bytes, slot_bytes;
+  __device__ void operator()(int64_t item, const char*& s, char*& d, u32& bytes) const {
+    const int q = static_cast<int>(item / n_runs);
+    const int run = static_cast<int>(item % n_runs);
+    const int4 t = tasks[q];
+    bytes = static_cast<u32>(t.z * slot_bytes);
+    s = pool + t.x * block_bytes + run * run_bytes;
+    d = const_cast<char*>(pool) + t.y * block_bytes + run * run_bytes;
+  }
+};
+
+__global__ void __launch_bounds__(32) kv_cow_bulk_kernel(CowMap map, const int32_t* task_count, int32_t* cow_ticket,
+                                                         int32_t* task_count_rw, int* status) {
+  const int64_t n_items = static_cast<int64_t>(*task_count) * map.n_runs;
+  bulk_copy_items(map, n_items, status);
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(cow_ticket, 1) == static_cast<int>(gridDim.x) - 1) {
+      *task_count_rw = 0;
+      *cow_ticket = 0;
+    }
+  }
+}
+
+__global__ void kv_cow_plain_kernel(CowMap map, int32_t* task_count, int32_t* cow_ticket) {
+  const int64_t n_items = static_cast<int64_t>(*task_count) * map.n_runs;
+  for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
+    const char* s;
+    char* d;
+    u32 bytes;
+    map(item, s, d, bytes);
+    for (u32 i = threadIdx.x; i < bytes; i += blockDim.x) d[i] = s[i];
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(cow_ticket, 1) == static_cast<int>(gridDim.x) - 1) {
+      *task_count = 0;
+      *cow_ticket = 0;
+    }
+  }
+}
+
+int launch_kv_paged_cow(const PagedArgs& a, bool bulk_ok, int num_sms, cudaStream_t s) {
+  const int n_runs = a.L * 2 * a.H;
+  const int64_t run_bytes = static_cast<int64_t>(a.block) * a.slot_bytes;
+  CowMap m{a.pool, a.tasks, n_runs, a.block_bytes, run_bytes, a.slot_bytes};
+  const int grid = num_sms * KV_CTAS_PER_SM;
+  if (bulk_ok && run_bytes <= KV_CHUNK) {
+    const size_t smem = static_cast<size_t>(KV_STAGES) * KV_CHUNK;
+    static bool attr_set = false;
+    if (!attr_set) {
+      cudaFuncSetAttribute(kv_cow_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+      attr_set = true;
+    }
+    kv_cow_bulk_kernel<<<grid, 32, smem, s>>>(m, a.task_count, a.cow_ticket, a.task_count, a.status);
+  } else {
+    kv_cow_plain_kernel<<<grid, 256, 0, s>>>(m, a.task_count, a.cow_ticket);
+  }
+  return cudaGetLastError() == cudaSuccess ? VBS_OK : VBS_ECUDA;
+}
+
+}  // namespace vbs
