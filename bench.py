@@ -240,7 +240,7 @@ def run_ours(args, rank, local_rank, world):
             if ev is not None:
                 ev[2].record(stream)
             state["t"] += 1
-            state["launches"] += 3
+            state["launches"] += 4
             if st:
                 raise RuntimeError(f"step failed: {st}")
 
@@ -306,7 +306,7 @@ def run_ours(args, rank, local_rank, world):
         "clocks": clk,
     }
     rec = recorded_traffic("bs_step_kernel")
-    out["roofline"] = {"kernel": "bs_step_kernel", "bound": "hbm", "achieved": round(ach_bs, 1),
+    out["roofline"] = {"kernel": "bs_stream_kernel + bs_merge_kernel", "bound": "hbm", "achieved": round(ach_bs, 1),
                        "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                        "frac": round(ach_bs / peak, 4),
                        "traffic": rec["dram_bytes_per_launch"] if rec else None,
@@ -566,6 +566,52 @@ def run_reference(args, rank, world):
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_profile(kernel: str):
+    """A few launches of one kernel on its workload, for ncu (inputs > L2, a few GB at most)."""
+    import torch
+
+    import synth
+    import verify_bs_step_gb300 as vbs
+    from verify_bs_step_gb300 import _build
+
+    _build.build()
+    dev = torch.device("cuda", 0)
+    wl = WORKLOAD
+    if kernel == "bs_step":
+        B, W, V, T = wl["B"], wl["W"], wl["V"], wl["T"]
+        ring = make_logits_ring(torch, synth, 3, wl["seed"], dev, B, W, V)
+        bs = vbs.BeamSearch(B, W, V, eos=wl["eos"], alpha=wl["alpha"], max_len=T, dtype=torch.bfloat16, device=dev)
+        for i in range(8):
+            bs.step(ring[i % 3])
+        bs.close()
+    elif kernel == "bpd_verify":
+        B, k, V = 256, 8, 32000
+        base, props, heads = synth.geometric_prefix_proposals(B, k, V, seed=500, step=0)
+        logits = synth.planted_rows(heads.to(dev), V, seed=500, salt=0, device=dev)
+        pr = props.to(torch.int32).to(dev)
+        for _ in range(6):
+            vbs.bpd_verify(logits, pr)
+    elif kernel == "kv_paged":
+        B, W, V, T, P = wl["B"], wl["W"], wl["V"], wl["T"], wl["P"]
+        L, H, D, blk = wl["L"], wl["H"], wl["D"], wl["block"]
+        ring = make_logits_ring(torch, synth, 3, wl["seed"], dev, B, W, V)
+        bs = vbs.BeamSearch(B, W, V, eos=wl["eos"], alpha=wl["alpha"], max_len=T, dtype=torch.bfloat16, device=dev)
+        S = -(-P // blk) + W * (-(-T // blk) + 2)
+        MB = -(-(P + T + 1) // blk) + 1
+        pk = vbs.PagedKV(B, W, L, H, D, blocks_per_sentence=S, max_blocks=MB, block=blk, device=dev)
+        pk.prefill(P)
+        pk.prepare(P)
+        for i in range(8):
+            bi, _, _ = bs.step(ring[i % 3])
+            pk.reorder(bi, P + i)
+        bs.close()
+        pk.close()
+    else:
+        raise SystemExit(f"unknown kernel {kernel}")
+    torch.cuda.synchronize()
+    print(f"profile run of {kernel}: ok")
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -574,7 +620,11 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true", help="skip the secondary lines")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle time budget for cpu_baseline")
+    ap.add_argument("--profile", default=None, help="run a few launches of one kernel (for ncu) and exit")
     args = ap.parse_args(argv)
+    if args.profile:
+        run_profile(args.profile)
+        return
     rank, local_rank, world = dist_env()
     if world > 1:
         import torch

@@ -85,10 +85,10 @@ typedef struct vbs_bs vbs_bs;
  *   bos, pad       the BOS token of column 0 and the PAD token of finished rows
  *   dtype          VBS_F32 or VBS_BF16 logits
  *   stream         the stream all of this context's work is enqueued on
- * Limits: 1 <= W <= 16, V >= 2, batch >= 1, R*V < 2^31, 1 <= max_len.
+ * Limits: 1 <= W <= 16, V >= 2, 1 <= batch <= 32767, R*V < 2^31, 1 <= max_len.
  * Errors: VBS_EINVAL, VBS_ENOMEM, VBS_ECUDA.  *ctx is NULL on error.
  */
-int bs_init(vbs_bs** ctx, int batch, int W, int V, int eos, float alpha, int early_stopping, int lp_kind,
+int bs_init(vbs_bs** ctx, int batch, int W, int V, int eos, double alpha, int early_stopping, int lp_kind,
             int max_len, int bos, int pad, int dtype, vbs_stream_t stream);
 
 /*

@@ -30,7 +30,7 @@ _pp = ctypes.POINTER(ctypes.c_void_p)
 SIGNATURES = {
     "vbs_strerror": (ctypes.c_char_p, [_c_int]),
     "vbs_version": (_c_int, []),
-    "bs_init": (_c_int, [_pp, _c_int, _c_int, _c_int, _c_int, _c_f, _c_int, _c_int, _c_int, _c_int, _c_int,
+    "bs_init": (_c_int, [_pp, _c_int, _c_int, _c_int, _c_int, ctypes.c_double, _c_int, _c_int, _c_int, _c_int, _c_int,
                          _c_int, _vp]),
     "bs_reset": (_c_int, [_vp, _vp, _vp]),
     "bs_step": (_c_int, [_vp, _vp, _c_i64, _vp, _vp, _vp, _vp, _vp]),

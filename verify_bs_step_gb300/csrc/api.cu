@@ -1,6 +1,7 @@
 // The C ABI of libvbs: argument checks, context lifetime, workspace layout and
 // kernel launches.  No entry point after an init allocates device memory.
 
+#include <cmath>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -27,6 +28,12 @@ int num_sms() {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// lp(|y|) of "9.2 贪心搜索与束搜索" §9.2.3: GNMT ((5 + |y|) / 6)^alpha or |y|^alpha; alpha = 0 gives 1.
+double length_penalty(int n, double alpha, int kind) {
+  if (alpha == 0.0) return 1.0;
+  return kind == VBS_LP_GNMT ? std::pow((5.0 + n) / 6.0, alpha) : std::pow(static_cast<double>(n), alpha);
+}
 
 // One device allocation carved into 256-byte aligned pieces.
 struct Carver {
@@ -84,11 +91,12 @@ VBS_EXPORT int vbs_version(void) { return 100; }
 // beam search
 // =====================================================================================
 
-VBS_EXPORT int bs_init(vbs_bs** out, int batch, int W, int V, int eos, float alpha, int early_stopping,
+VBS_EXPORT int bs_init(vbs_bs** out, int batch, int W, int V, int eos, double alpha, int early_stopping,
                        int lp_kind, int max_len, int bos, int pad, int dtype, vbs_stream_t stream) {
   if (!out) return VBS_EINVAL;
   *out = nullptr;
-  if (batch < 1 || W < 1 || W > vbs::WMAX || V < 2 || max_len < 1) return VBS_EINVAL;
+  if (batch < 1 || batch > 32767 || W < 1 || W > vbs::WMAX || V < 2 || max_len < 1) return VBS_EINVAL;
+  if (!(alpha == alpha)) return VBS_EINVAL;
   if (dtype != VBS_F32 && dtype != VBS_BF16) return VBS_EINVAL;
   if (lp_kind != VBS_LP_GNMT && lp_kind != VBS_LP_POWER) return VBS_EINVAL;
   if (early_stopping < VBS_ES_FALSE || early_stopping > VBS_ES_NEVER) return VBS_EINVAL;
@@ -112,14 +120,14 @@ VBS_EXPORT int bs_init(vbs_bs** out, int batch, int W, int V, int eos, float alp
   a.early_stopping = early_stopping;
   a.lp_kind = lp_kind;
   a.max_len = max_len;
-  a.alpha = static_cast<double>(alpha);
+  a.alpha = alpha;
   c->stream = reinterpret_cast<cudaStream_t>(stream);
 
-  // the flat split: a whole number of 2-CTA-per-SM waves, ranges of >= 4096 elements,
+  // the flat split: one wave of resident CTAs, ranges of >= 4096 elements,
   // and few enough partials per row for one merge (P * K <= PART_KEYS)
   const int VEC = dtype == VBS_BF16 ? 8 : 4;
   const int64_t total = R * V;
-  int64_t G = std::min<int64_t>(static_cast<int64_t>(num_sms()) * 2, (total + 4095) / 4096);
+  int64_t G = std::min<int64_t>(static_cast<int64_t>(num_sms()) * vbs::bs_ctas_per_sm(), (total + 4095) / 4096);
   G = std::max<int64_t>(G, 1);
   int64_t per = (total + G - 1) / G;
   const int64_t pmax = vbs::PART_KEYS / a.K - 1;
@@ -137,9 +145,9 @@ VBS_EXPORT int bs_init(vbs_bs** out, int batch, int W, int V, int eos, float alp
     a.part_key = cv.take<u64>(R * a.P * a.K);
     a.row_lse = cv.take<double>(R);
     a.row_key = cv.take<u64>(R * a.K);
-    a.row_ticket = cv.take<int>(R);
-    a.sent_ticket = cv.take<int>(batch);
-    a.glob_ticket = cv.take<int>(1);
+    a.row_p0 = cv.take<int>(R);
+    a.row_np = cv.take<int>(R);
+    a.done_count = cv.take<int>(1);
     a.all_done_dev = cv.take<int32_t>(1);
     a.status = cv.take<int>(1);
     a.done = cv.take<int>(batch);
@@ -163,7 +171,17 @@ VBS_EXPORT int bs_init(vbs_bs** out, int batch, int W, int V, int eos, float alp
       cv.base = static_cast<char*>(p);
     }
   }
-  if (cudaMemsetAsync(c->dev_block, 0, cv.off, c->stream) != cudaSuccess) {
+  // which CTAs hold each row: row r spans elements [r V, (r + 1) V) of the flat split
+  std::vector<int> p0(R), np(R);
+  for (int64_t r = 0; r < R; ++r) {
+    p0[r] = static_cast<int>((r * V) / per);
+    np[r] = static_cast<int>(((r + 1) * V - 1) / per - (r * V) / per + 1);
+  }
+  bool ok = cudaMemsetAsync(c->dev_block, 0, cv.off, c->stream) == cudaSuccess;
+  ok = ok && cudaMemcpyAsync(a.row_p0, p0.data(), R * sizeof(int), cudaMemcpyHostToDevice, c->stream) == cudaSuccess;
+  ok = ok && cudaMemcpyAsync(a.row_np, np.data(), R * sizeof(int), cudaMemcpyHostToDevice, c->stream) == cudaSuccess;
+  ok = ok && cudaStreamSynchronize(c->stream) == cudaSuccess;
+  if (!ok) {
     cudaFree(c->dev_block);
     delete c;
     return VBS_ECUDA;
@@ -203,6 +221,9 @@ VBS_EXPORT int bs_step(vbs_bs* c, const void* logits, int64_t ld, float* scores,
   a.tokens = tokens;
   a.all_done_out = all_done;
   a.t = c->step + 1;
+  a.lp_t = length_penalty(a.t, a.alpha, a.lp_kind);
+  a.lp_bound = (a.early_stopping == VBS_ES_NEVER && a.alpha > 0.0) ? length_penalty(a.max_len, a.alpha, a.lp_kind)
+                                                                   : a.lp_t;
   const int es = a.dtype == VBS_BF16 ? 2 : 4;
   const int VEC = 16 / es;
   const bool vec_ok = aligned16(logits) && (ld * es) % 16 == 0 && a.V % VEC == 0;
@@ -220,6 +241,7 @@ VBS_EXPORT int bs_finalize(vbs_bs* c, const float* scores, const int32_t* seqs, 
   if (sq != c->seqs_bound) return VBS_ESTATE;
   vbs::BsArgs a = c->a;
   a.t = c->step;
+  a.lp_t = length_penalty(a.t, a.alpha, a.lp_kind);
   return vbs::launch_bs_finalize(a, scores, sq, out_seqs, out_len, out_score, c->stream);
 }
 

@@ -8,7 +8,8 @@ namespace vbs {
 
 constexpr int WMAX = 16;          // beams per sentence
 constexpr int KMAX = 2 * WMAX;    // candidates kept per row (2W)
-constexpr int PART_KEYS = 512;    // keys one row merge can hold (partials x K)
+constexpr int PART_KEYS = 256;    // keys one row merge can hold (partials x K)
+constexpr int CAND_CAP = 288;     // candidate buffer per warp: K + one 32-lane x 8-element vector
 
 struct BsArgs {
   const void* logits;
@@ -24,18 +25,20 @@ struct BsArgs {
   int32_t* tokens;
   int32_t* all_done_out;          // optional, caller's
   int32_t* all_done_dev;          // the context's own flag
-  int t;                          // 1-based step number
+  int t;                          // 1-based step number (finalize: steps run)
   int eos, bos, pad, early_stopping, lp_kind, max_len;
   double alpha;
+  double lp_t;                    // lp(t): normalises an EOS hit of this step (finalize: lp(steps run))
+  double lp_bound;                // lp of the stopping test's best attainable length
   // workspace
   float* part_M;
   float* part_l;
   unsigned long long* part_key;
   double* row_lse;
   unsigned long long* row_key;
-  int* row_ticket;
-  int* sent_ticket;
-  int* glob_ticket;
+  int* row_p0;                    // [R] the first CTA whose range holds row r
+  int* row_np;                    // [R] the number of CTAs (partials) holding row r
+  int* done_count;                // sentences finished (step-local counter)
   int* done;
   // finished sets
   double* fin_ns;
@@ -53,6 +56,7 @@ int launch_bs_reset(const BsArgs& a, cudaStream_t s);
 int launch_bs_finalize(const BsArgs& a, const float* scores, const int32_t* seqs, int32_t* out_seqs,
                        int32_t* out_len, float* out_score, cudaStream_t s);
 int bs_threads_per_cta();
+int bs_ctas_per_sm();
 
 // KV reorder
 struct KvGeom {

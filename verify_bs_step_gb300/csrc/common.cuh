@@ -65,6 +65,32 @@ template <> struct Vec16<float> {
   }
 };
 
+// Elementwise max of two packed bf16 pairs (PTX max.bf16x2).
+__device__ __forceinline__ u32 max_bf16x2(u32 a, u32 b) {
+  u32 d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// The largest value held in one 16-byte vector word set (bf16 or fp32), as fp32.
+template <typename T> struct VecMax;
+template <> struct VecMax<bf16_t> {
+  static constexpr u32 NEG = 0xff80ff80u;           // two bf16 -inf
+  __device__ __forceinline__ static u32 fold(const uint4& q, u32 acc) {
+    return max_bf16x2(max_bf16x2(acc, max_bf16x2(q.x, q.y)), max_bf16x2(q.z, q.w));
+  }
+  __device__ __forceinline__ static float finish(u32 acc) { return fmaxf(bf16_lo(acc), bf16_hi(acc)); }
+};
+template <> struct VecMax<float> {
+  static constexpr u32 NEG = 0xff800000u;           // fp32 -inf
+  __device__ __forceinline__ static u32 fold(const uint4& q, u32 acc) {
+    float m = fmaxf(fmaxf(__uint_as_float(acc), __uint_as_float(q.x)),
+                    fmaxf(__uint_as_float(q.y), fmaxf(__uint_as_float(q.z), __uint_as_float(q.w))));
+    return __float_as_uint(m);
+  }
+  __device__ __forceinline__ static float finish(u32 acc) { return __uint_as_float(acc); }
+};
+
 // ------------------------------------------------------------------------------------
 // arithmetic
 // ------------------------------------------------------------------------------------
@@ -181,8 +207,21 @@ __device__ __forceinline__ void mbar_expect_tx(u64* bar, u32 bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
                :: "r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
+__device__ __forceinline__ void mbar_arrive(u64* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_u32(bar)) : "memory");
+}
+// Barrier among the first `nthreads` threads of the CTA (named barrier `id`, not 0).
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
+}
+// Device-scope atomic add with acquire-release ordering; returns the old value.
+__device__ __forceinline__ int atomic_add_acq_rel(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
 // Bounded wait on phase `parity`; returns false if it gave up.
-__device__ __forceinline__ bool mbar_wait(u64* bar, u32 parity, u32 max_iter = 1u << 26) {
+__device__ __forceinline__ bool mbar_wait(u64* bar, u32 parity, u32 max_iter = 1u << 22) {
   u32 ok = 0;
   for (u32 i = 0; i < max_iter; ++i) {
     asm volatile(
