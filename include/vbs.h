@@ -52,7 +52,8 @@ enum {
   VBS_ESTATE = -4,   /* the call does not fit the context's state (e.g. more than max_len steps) */
   VBS_EALIGN = -5,   /* a pointer or stride is not aligned as the call needs */
   VBS_ETIMEOUT = -6, /* a bounded device-side wait gave up */
-  VBS_EINPUT = -7    /* the input data broke a precondition (NaN / +inf logits, ...) */
+  VBS_EINPUT = -7,   /* the input data broke a precondition (NaN / +inf logits, ...) */
+  VBS_ESCRATCH = -8  /* the problem is larger than bs_expand_static's static scratch allows */
 };
 
 enum { VBS_F32 = 0, VBS_BF16 = 1 };
@@ -158,6 +159,38 @@ int bs_steps(vbs_bs* ctx, int* steps);
 int bs_status(vbs_bs* ctx);
 /* Free the context (synchronises its stream first). NULL is a no-op. */
 int bs_destroy(vbs_bs* ctx);
+
+/*
+ * One beam expansion with no context and no allocation.  The pages have no
+ * counterpart: this exists for callers that cannot allocate device memory --
+ * code running inside an allocator or a memory-pool callback, a host whose
+ * memory budget is fixed up front, or an embedding runtime that forbids
+ * cudaMalloc after start-up.
+ *
+ * Computes, for every sentence b of `batch` sentences of W beams, the W best
+ * of log_softmax(logits[r, :]) + scores_in[r] over its W*V candidates, ranked
+ * by (score desc, flat index j = w*V + v asc): exactly the beams bs_step would
+ * keep when no token ends a hypothesis (eos = -1) and no sentence is finished.
+ *   logits     [batch*W, V] device, row stride ld >= V elements, dtype VBS_*
+ *   scores_in  [batch*W] device fp32 cumulative scores; a row at -inf is not read
+ *   scores_out [batch*W] device fp32 new scores (may equal scores_in)
+ *   beam_idx   [batch*W] device int32 global parent row; tokens [batch*W] int32
+ * Scratch: a static device array of 4 MiB (the partial sums, partial top-K
+ * lists and row maps), which every process that loads the library holds on
+ * each device it uses until it exits.  Limit: batch*W <= 8192 rows (then the
+ * scratch always fits), 1 <= W <= 16, V >= 2, batch*W*V < 2^31; larger
+ * problems return VBS_ESCRATCH before anything is launched.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  The call allocates nothing and frees nothing.  Every call shares
+ * the one array and leaves its contents behind; each call rewrites what it
+ * reads, but two calls that overlap on the GPU (different streams, or
+ * different host threads) race on it and must be serialised by the caller.
+ * Device-side errors go to the status word that vbs_stateless_status() reads.
+ * Errors: VBS_EINVAL, VBS_ESCRATCH, VBS_ECUDA.
+ */
+int bs_expand_static(const void* logits, int64_t ld, int batch, int W, int V, int dtype, const float* scores_in,
+                     float* scores_out, int32_t* beam_idx, int32_t* tokens, vbs_stream_t stream);
 
 /* =============================================================================
  * KV-cache reorder ([LM] §9.2.2 KV paragraph; [LS] cache refresh)

@@ -19,7 +19,7 @@ __all__ = ["BeamSearch", "PagedKV", "kv_reorder", "bpd_propose", "bpd_verify", "
 F32, BF16 = 0, 1
 LP_GNMT, LP_POWER = 0, 1
 ES_FALSE, ES_TRUE, ES_NEVER = 0, 1, 2
-OK, EINVAL, ECUDA, ENOMEM, ESTATE, EALIGN, ETIMEOUT, EINPUT = 0, -1, -2, -3, -4, -5, -6, -7
+OK, EINVAL, ECUDA, ENOMEM, ESTATE, EALIGN, ETIMEOUT, EINPUT, ESCRATCH = 0, -1, -2, -3, -4, -5, -6, -7, -8
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libvbs.so")
 
@@ -40,6 +40,7 @@ SIGNATURES = {
     "bs_steps": (_c_int, [_vp, ctypes.POINTER(_c_int)]),
     "bs_status": (_c_int, [_vp]),
     "bs_destroy": (_c_int, [_vp]),
+    "bs_expand_static": (_c_int, [_vp, _c_i64, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _vp, _vp, _vp]),
     "kv_reorder": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _vp]),
     "vbs_stateless_status": (_c_int, [_vp]),
     "kv_paged_init": (_c_int, [_pp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp]),
@@ -192,6 +193,35 @@ class BeamSearch:
             self.close()
         except Exception:
             pass
+
+
+def bs_expand_static(logits: torch.Tensor, scores_in: torch.Tensor, W: int, scores_out: torch.Tensor | None = None,
+                     beam_idx: torch.Tensor | None = None, tokens: torch.Tensor | None = None):
+    """One beam expansion (no end-of-sequence token) through the allocation-free entry point.
+
+    logits: CUDA [batch*W, V] (row stride may exceed V), float32 or bfloat16; scores_in: float32
+    [batch*W].  Returns (beam_idx, tokens, scores_out).  The library itself allocates nothing;
+    the output tensors this wrapper creates when none are given are torch's.
+    """
+    if logits.dim() != 2 or logits.stride(1) != 1:
+        raise ValueError("logits must be [rows, V] with unit column stride")
+    R, V = logits.shape
+    if W < 1 or R % W:
+        raise ValueError("rows must be a multiple of W")
+    dev = logits.device
+    if scores_out is None:
+        scores_out = torch.empty(R, dtype=torch.float32, device=dev)
+    if beam_idx is None:
+        beam_idx = torch.empty(R, dtype=torch.int32, device=dev)
+    if tokens is None:
+        tokens = torch.empty(R, dtype=torch.int32, device=dev)
+    _check(lib().bs_expand_static(_dev_ptr(logits, "logits"), logits.stride(0), R // W, W, V,
+                                  _dtype_code(logits.dtype), _dev_ptr(scores_in, "scores_in", torch.float32),
+                                  _dev_ptr(scores_out, "scores_out", torch.float32),
+                                  _dev_ptr(beam_idx, "beam_idx", torch.int32),
+                                  _dev_ptr(tokens, "tokens", torch.int32), _stream(dev)),
+           "bs_expand_static")
+    return beam_idx, tokens, scores_out
 
 
 class _KvDesc(ctypes.Structure):

@@ -81,6 +81,7 @@ VBS_EXPORT const char* vbs_strerror(int status) {
     case VBS_EALIGN: return "misaligned pointer or stride";
     case VBS_ETIMEOUT: return "a bounded device-side wait gave up";
     case VBS_EINPUT: return "input data broke a precondition";
+    case VBS_ESCRATCH: return "problem too large for the static scratch of bs_expand_static";
     default: return "unknown status";
   }
 }
@@ -293,6 +294,48 @@ VBS_EXPORT int bs_destroy(vbs_bs* c) {
   cudaFree(c->dev_block);
   delete c;
   return VBS_OK;
+}
+
+// One expansion step whose scratch is a static device array (no allocation).
+VBS_EXPORT int bs_expand_static(const void* logits, int64_t ld, int batch, int W, int V, int dtype,
+                                const float* scores_in, float* scores_out, int32_t* beam_idx, int32_t* tokens,
+                                vbs_stream_t stream) {
+  if (!logits || !scores_in || !scores_out || !beam_idx || !tokens) return VBS_EINVAL;
+  if (batch < 1 || W < 1 || W > vbs::WMAX || V < 2 || ld < V) return VBS_EINVAL;
+  if (dtype != VBS_F32 && dtype != VBS_BF16) return VBS_EINVAL;
+  const int64_t R = static_cast<int64_t>(batch) * W;
+  if (R > vbs::STATIC_MAX_ROWS) return VBS_ESCRATCH;
+  if (R * V >= (int64_t{1} << 31)) return VBS_EINVAL;
+  vbs::BsArgs a{};
+  a.logits = logits;
+  a.ld = ld;
+  a.dtype = dtype;
+  a.B = batch;
+  a.W = W;
+  a.V = V;
+  a.K = 2 * W;
+  a.R = static_cast<int>(R);
+  a.eos = -1;
+  a.scores = const_cast<float*>(scores_in);
+  a.beam_idx = beam_idx;
+  a.tokens = tokens;
+  // the same flat split as bs_init
+  const int VEC = dtype == VBS_BF16 ? 8 : 4;
+  const int64_t total = R * V;
+  int64_t G = std::min<int64_t>(static_cast<int64_t>(num_sms()) * vbs::bs_ctas_per_sm(), (total + 4095) / 4096);
+  G = std::max<int64_t>(G, 1);
+  int64_t per = (total + G - 1) / G;
+  const int64_t pmax = vbs::PART_KEYS / a.K - 1;
+  per = std::max(per, (V + pmax - 1) / pmax);
+  per = (per + VEC - 1) / VEC * VEC;
+  G = (total + per - 1) / per;
+  a.per = per;
+  a.P = static_cast<int>((V + per - 1) / per + 1);
+  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&a.status), g_stateless_status) != cudaSuccess) return VBS_ECUDA;
+  const int es = dtype == VBS_BF16 ? 2 : 4;
+  const bool vec_ok = aligned16(logits) && (ld * es) % 16 == 0 && V % VEC == 0;
+  return vbs::launch_bs_expand_static(a, static_cast<int>(G), vec_ok, scores_out,
+                                      reinterpret_cast<cudaStream_t>(stream));
 }
 
 // =====================================================================================

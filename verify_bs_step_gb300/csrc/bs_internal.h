@@ -58,6 +58,11 @@ int launch_bs_finalize(const BsArgs& a, const float* scores, const int32_t* seqs
 int bs_threads_per_cta();
 int bs_ctas_per_sm();
 
+// bs_expand_static: scratch in a static device array of this size; rows at most
+constexpr size_t STATIC_SCRATCH_BYTES = size_t{4} << 20;
+constexpr int STATIC_MAX_ROWS = 8192;
+int launch_bs_expand_static(BsArgs a, int grid, bool vector_ok, float* scores_out, cudaStream_t s);
+
 // KV reorder
 struct KvGeom {
   int L, H, rows;

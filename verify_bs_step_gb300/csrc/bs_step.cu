@@ -30,6 +30,7 @@
 
 #include <cfloat>
 #include <cmath>
+#include <mutex>
 
 #include "common.cuh"
 #include "bs_internal.h"
@@ -890,5 +891,133 @@ int launch_bs_finalize(const BsArgs& a, const float* scores, const int32_t* seqs
 
 int bs_threads_per_cta() { return BS_NT; }
 int bs_ctas_per_sm() { return 1; }
+
+// ---------------------------------------------------------------------------------------
+// one expansion step without allocation: its scratch is a static device array
+// ---------------------------------------------------------------------------------------
+
+// The partials, row maps and done flags of bs_expand_static.  Every process that loads
+// the library holds this array on each device it touches, until it exits.
+static __device__ __align__(256) unsigned char g_static_scratch[STATIC_SCRATCH_BYTES];
+
+__global__ void bs_static_prep_kernel(const BsArgs a) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < a.R) {
+    const int64_t e0 = static_cast<int64_t>(i) * a.V;
+    const int64_t p0 = e0 / a.per;
+    a.row_p0[i] = static_cast<int>(p0);
+    a.row_np[i] = static_cast<int>((e0 + a.V - 1) / a.per - p0 + 1);
+  }
+  if (i < a.B) a.done[i] = 0;
+}
+
+// One CTA per sentence: the rows' partials merged as in bs_merge_kernel, then the W best
+// of the sentence's candidates by (score desc, flat index asc) become the new beams.
+__global__ void __launch_bounds__(MG_NT) bs_expand_merge_kernel(const BsArgs a, float* scores_out) {
+  extern __shared__ __align__(16) unsigned char mg_smem[];
+  MergeShared& sm = *reinterpret_cast<MergeShared*>(mg_smem);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int W = a.W, K = a.K;
+  const int r0 = blockIdx.x * W;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  for (int w = warp; w < W; w += MG_NW) row_merge(a, sm, r0 + w, w, lane);
+  if (tid < W) { sm.sel_w[tid] = 0; sm.sel_i[tid] = 0; sm.sel_c[tid] = -INFINITY; }
+  __syncthreads();
+  for (int f = tid; f < W * K; f += MG_NT) {
+    const int w = f / K, i = f - w * K;
+    if (i >= sm.nval[w]) continue;
+    const float c = sm.candv[f];
+    int rank = i;
+    for (int w2 = 0; w2 < W && rank < W; ++w2)
+      if (w2 != w) rank += count_better(sm.candv + w2 * K, sm.nval[w2], c, w2 < w);
+    if (rank < W) {
+      sm.sel_w[rank] = w;
+      sm.sel_i[rank] = i;
+      sm.sel_c[rank] = c;
+    }
+  }
+  __syncthreads();
+  if (tid < W) {
+    const int w = sm.sel_w[tid];
+    a.beam_idx[r0 + tid] = r0 + w;
+    a.tokens[r0 + tid] = static_cast<int32_t>(key_v(sm.wtop[w * K + sm.sel_i[tid]]));
+    scores_out[r0 + tid] = sm.sel_c[tid];
+  }
+}
+
+namespace {
+constexpr int MAX_DEVICES = 256;
+std::mutex g_static_mu;
+void* g_static_addr[MAX_DEVICES];   // the array's device address, per device ordinal
+}  // namespace
+
+int launch_bs_expand_static(BsArgs a, int grid, bool vector_ok, float* scores_out, cudaStream_t s) {
+  // carve the array: offsets first, so that an oversized problem is refused before any CUDA call
+  size_t off = 0;
+  auto take = [&off](size_t bytes) {
+    off = (off + 255) & ~static_cast<size_t>(255);
+    const size_t at = off;
+    off += bytes;
+    return at;
+  };
+  const size_t RP = static_cast<size_t>(a.R) * a.P;
+  const size_t o_M = take(RP * sizeof(float));
+  const size_t o_l = take(RP * sizeof(float));
+  const size_t o_key = take(RP * a.K * sizeof(u64));
+  const size_t o_p0 = take(static_cast<size_t>(a.R) * sizeof(int));
+  const size_t o_np = take(static_cast<size_t>(a.R) * sizeof(int));
+  const size_t o_done = take(static_cast<size_t>(a.B) * sizeof(int));
+  if (off > STATIC_SCRATCH_BYTES) return VBS_ESCRATCH;
+
+  // set-up, once per device, with that device current: the array's device address
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return VBS_ECUDA;
+  char* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!g_static_addr[dev]) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return VBS_ECUDA;
+      g_static_addr[dev] = p;
+    }
+    base = static_cast<char*>(g_static_addr[dev]);
+  }
+  a.part_M = reinterpret_cast<float*>(base + o_M);
+  a.part_l = reinterpret_cast<float*>(base + o_l);
+  a.part_key = reinterpret_cast<u64*>(base + o_key);
+  a.row_p0 = reinterpret_cast<int*>(base + o_p0);
+  a.row_np = reinterpret_cast<int*>(base + o_np);
+  a.done = reinterpret_cast<int*>(base + o_done);
+
+  const int n = a.R > a.B ? a.R : a.B;
+  bs_static_prep_kernel<<<(n + 255) / 256, 256, 0, s>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return VBS_ECUDA;
+  int st;
+  if (a.dtype == VBS_BF16)
+    st = vector_ok ? launch_stream<bf16_t, true>(a, grid, s) : launch_stream<bf16_t, false>(a, grid, s);
+  else
+    st = vector_ok ? launch_stream<float, true>(a, grid, s) : launch_stream<float, false>(a, grid, s);
+  if (st != VBS_OK) return st;
+
+  static bool attr_set = false;
+  const int smem = static_cast<int>(sizeof(MergeShared));
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(bs_expand_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+      return VBS_ECUDA;
+    attr_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.B);
+  cfg.blockDim = dim3(MG_NT);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, bs_expand_merge_kernel, a, scores_out) == cudaSuccess ? VBS_OK : VBS_ECUDA;
+}
 
 }  // namespace vbs
