@@ -40,13 +40,14 @@ namespace vbs {
 constexpr int BS_NC = 512;                        // consumer threads
 constexpr int BS_NCW = BS_NC / 32;                // consumer warps
 constexpr int BS_NT = BS_NC + 32;                 // + the producer warp
-constexpr int BS_NW = BS_NT / 32;
 constexpr int BS_U = 4;                           // 16-byte vectors per consumer per chunk
 constexpr int STAGE_BYTES = BS_NC * BS_U * 16;    // 32 KiB
 constexpr int NSTAGE = 6;
-constexpr int QCAP = 1024;                        // the CTA's candidate queue (one row segment)
-constexpr int QREFRESH = 16;                      // threshold refresh every QREFRESH pushes ...
-constexpr int QREFRESH_MAX = 128;                 // ... while the queue holds at most this many
+constexpr int NSLOT = 4;                          // row segments held before they are published
+constexpr int QSEG = 512;                         // candidate queue of one segment
+constexpr int QSTEP = 8;                          // threshold refresh once QSTEP more keys are queued
+constexpr int FIN_CAP = 256;                      // keys collected at a segment's final bar
+constexpr int CT_CAP = 64;                        // tiles re-read at a segment's final bar
 constexpr int SEQ_TILE_INTS = 2048;               // sequence gather tile (all W rows)
 constexpr int BAR_CONSUMERS = 1;                  // named barrier of the consumer warps
 constexpr int MG_NT = 256;                        // merge kernel threads
@@ -78,20 +79,6 @@ __device__ void warp_select_topk(u64* keys, int n, int K, u64* out, int lane) {
     if (lane == 0) out[round] = g;
     __syncwarp();
   }
-}
-
-// K best of n unsorted keys by counting ranks (small n; keys unique, 0 = empty).
-__device__ void warp_rank_topk(const u64* keys, int n, int K, u64* out, int lane) {
-  if (lane < K) out[lane] = 0;
-  __syncwarp();
-  for (int j = lane; j < n; j += 32) {
-    const u64 k = keys[j];
-    if (k == 0) continue;
-    int rank = 0;
-    for (int q = 0; q < n; ++q) rank += keys[q] > k;
-    if (rank < K) out[rank] = k;
-  }
-  __syncwarp();
 }
 
 // Number of entries of a descending list L[0..len) greater than k.
@@ -127,14 +114,19 @@ __device__ void warp_merge_sorted(const u64* lists, int nl, int K, u64* out, int
 
 struct BsShared {                              // the stream kernel
   unsigned char ring[NSTAGE][STAGE_BYTES];     // the streamed chunks
-  u64 q[QCAP];                                 // candidate keys of the current row segment
-  u64 lbk[BS_NC];                              // first-tile lower bounds (threshold seed)
-  u64 pool[64];
-  u64 ptop[KMAX];                              // a partial's top K
+  u64 q[NSLOT][QSEG];                          // hot tiles (max, position) per row segment; keys after a rescan
+  u64 fin[NSLOT][FIN_CAP];                     // a segment's final candidate keys
+  u32 ctile[NSLOT][CT_CAP];                    // a segment's final candidate tiles
+  float M[NSLOT][BS_NCW], l[NSLOT][BS_NCW];    // per-warp (max, scaled sum) of each segment
   u64 full[NSTAGE], empty[NSTAGE];
-  u64 thr;                                     // CTA threshold key
-  int qcnt, ovf;
-  float M[BS_NCW], l[BS_NCW];
+  u64 rbar[NSLOT];                             // the key bar of a rescan
+  u32 thr[NSLOT];                              // threshold (ordered logit bits) per segment
+  u32 sbar[NSLOT];                             // the final bar (ordered logit bits)
+  int qcnt[NSLOT];                             // entries reserved in q[slot] (> QSEG: overflow)
+  int qref[NSLOT];                             // qcnt at the last threshold refresh
+  int fcnt[NSLOT];                             // keys found at the final bar
+  int mode[NSLOT];                             // 0: tiles resolved, 1: needs a rescan, 2: q holds keys
+  int seg_r[NSLOT], seg_v0[NSLOT], seg_v1[NSLOT], seg_skip[NSLOT];
 };
 
 struct MergeShared {                           // the merge kernel
@@ -156,36 +148,59 @@ struct MergeShared {                           // the merge kernel
 };
 
 // ---------------------------------------------------------------------------------------
-// the candidate queue
+// thresholds and the hot-tile queues
 // ---------------------------------------------------------------------------------------
+//
+// A lane whose tile (BS_U vectors of one chunk) has a maximum at or above the segment's
+// threshold queues one entry: (ordered bits of the tile maximum, first column of the
+// tile).  Tile maxima are logits of distinct elements, so the K-th best queued maximum is
+// a lower bound of the segment's K-th best logit; the threshold only ever takes such
+// values.  At the end, every element at or above the final bar (the K-th best queued
+// maximum) lies in a queued tile whose maximum reaches the bar: only those few tiles are
+// read again, from global memory, to find the segment's exact K best keys.
 
-// Queue one key; true when the push completes a block of QREFRESH pushes.
-__device__ __forceinline__ bool queue_push(BsShared& sh, u64 key) {
-  const int pos = atomicAdd(&sh.qcnt, 1);
-  if (pos < QCAP) sh.q[pos] = key;
-  else sh.ovf = 1;
-  return (pos % QREFRESH) == QREFRESH - 1;
-}
-
-// Warp-wide: raise the CTA threshold to a key with K-1 queued keys above it.  Other
-// warps may be appending meanwhile: an entry not written yet reads 0 and is ignored,
-// and a key seen with K-1 larger keys always has K queued keys at or above it, so the
-// threshold never passes the segment's K-th best.
-__device__ __noinline__ void queue_refresh(BsShared& sh, int K, int lane) {
-  const volatile u64* vq = sh.q;
-  const int n = min(*reinterpret_cast<volatile int*>(&sh.qcnt), QCAP);
-  if (n < K || n > QREFRESH_MAX) return;
-  for (int j = lane; j < n; j += 32) {
-    const u64 k = vq[j];
-    if (k == 0) continue;
-    int rank = 0;
-    for (int i = 0; i < n; ++i) rank += vq[i] > k;
-    if (rank == K - 1) atomicMax(&sh.thr, k);
+// The rank of each lane's value among the warp's 32 (the lanes before it: a larger
+// value, or the same value in a lower lane); the ranks are 0..31, once each.
+__device__ __forceinline__ int warp_rank_u32(u32 v, int lane) {
+  int rank = 0;
+#pragma unroll
+  for (int i = 1; i < 32; ++i) {
+    const int src = (lane + i) & 31;
+    const u32 o = __shfl_sync(FULL, v, src);
+    rank += (o > v || (o == v && src < lane)) ? 1 : 0;
   }
+  return rank;
+}
+
+// The K-th largest of the warp's 32 lane values (repeats counted; K <= 32), 0 if fewer
+// than K lanes hold a nonzero value.
+__device__ __forceinline__ u32 warp_kth_u32(u32 v, int K, int lane) {
+  const u32 b = __ballot_sync(FULL, warp_rank_u32(v, lane) == K - 1);
+  return __shfl_sync(FULL, v, __ffs(b) - 1);
+}
+
+// Warp-wide: the K-th best of the lane maxima of the first n entries' tile maxima (0 if
+// fewer than K lanes hold one).  An entry another warp has reserved but not written yet
+// reads 0 and is ignored.
+__device__ __forceinline__ u32 queue_bar(const BsShared& sh, int slot, int n, int K, int lane) {
+  const volatile u64* vq = sh.q[slot];
+  u32 lm = 0;
+  for (int j = lane; j < n; j += 32) {
+    const u32 h = static_cast<u32>(vq[j] >> 32);
+    lm = h > lm ? h : lm;
+  }
+  return warp_kth_u32(lm, K, lane);
+}
+
+// Warp-wide: raise the segment's threshold from its queue.
+__device__ __noinline__ void queue_refresh(BsShared& sh, int slot, int n, int K, int lane) {
+  if (lane == 0) sh.qref[slot] = n;
+  const u32 t = queue_bar(sh, slot, n, K, lane);
+  if (lane == 0 && t) atomicMax(&sh.thr[slot], t);
 }
 
 // ---------------------------------------------------------------------------------------
-// pass 1
+// the stream kernel's parts
 // ---------------------------------------------------------------------------------------
 
 struct Chunk {
@@ -249,104 +264,196 @@ __device__ void produce(const BsArgs& a, BsShared& sh, int64_t e0, int64_t e1) {
   }
 }
 
-// Consumers, after a queue overflow: collect every key of the segment at or above
-// the K-th best queued so far, re-reading the segment from global memory, until one
-// pass fits in the queue.  Only adversarial orderings (e.g. ascending logits) get here.
-template <typename T>
-__device__ void rescan_segment(const BsArgs& a, BsShared& sh, int r, int64_t sv0, int64_t sv1) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int K = a.K;
-  const char* row = reinterpret_cast<const char*>(a.logits) + static_cast<int64_t>(r) * a.ld * Elem<T>::BYTES;
-  for (;;) {
-    if (warp == 0) {
-      warp_select_topk(sh.q, QCAP, K, sh.ptop, lane);
-      if (lane == 0) { sh.thr = sh.ptop[K - 1]; sh.qcnt = 0; sh.ovf = 0; }
-    }
-    named_sync(BAR_CONSUMERS, BS_NC);
-    for (int i = tid; i < QCAP; i += BS_NC) sh.q[i] = 0ull;
-    const u64 thr = sh.thr;
-    named_sync(BAR_CONSUMERS, BS_NC);
-    for (int64_t v = sv0 + tid; v < sv1; v += BS_NC) {
-      const u64 k = make_key(Elem<T>::load(row, v), static_cast<u32>(v));
-      if (k >= thr) queue_push(sh, k);
-    }
-    named_sync(BAR_CONSUMERS, BS_NC);
-    if (!sh.ovf) return;
-    named_sync(BAR_CONSUMERS, BS_NC);
-  }
-}
-
-// One lane's slow path: queue every element of its tile whose key reaches the
-// threshold.  Out of line, so the streaming loop stays small; the tile comes packed.
+// One warp: resolve segment s from its queue.  The final bar is the K-th best queued tile
+// maximum; the tiles reaching it are read again and every element at or above the bar
+// is collected into fin[s].  mode[s] becomes 1 when that does not fit (queue overflow,
+// more than CT_CAP tiles or FIN_CAP keys at the bar: ties, adversarial orders).
 template <typename T, int VEC>
-__device__ __noinline__ bool push_tile(BsShared& sh, uint4 q0, uint4 q1, uint4 q2, uint4 q3, u32 okmask, u32 vb,
-                                       float thr_x, u64 thr) {
-  bool crossed = false;
-  const uint4 qs[BS_U] = {q0, q1, q2, q3};
+__device__ void resolve_tiles(const BsArgs& a, BsShared& sh, int s, int lane) {
+  const int K = a.K;
+  const int qn = sh.qcnt[s];
+  const int n = min(qn, QSEG);
+  const u32 bar = queue_bar(sh, s, n, K, lane);
+  if (lane == 0) { sh.sbar[s] = bar; sh.fcnt[s] = 0; }
+  int nc = 0;
+  for (int j0 = 0; j0 < n; j0 += 32) {
+    const int j = j0 + lane;
+    const u64 e = j < n ? sh.q[s][j] : 0ull;
+    const bool cand = e != 0 && static_cast<u32>(e >> 32) >= bar;
+    const u32 b = __ballot_sync(FULL, cand);
+    const int pos = nc + __popc(b & ((1u << lane) - 1u));
+    if (cand && pos < CT_CAP) sh.ctile[s][pos] = static_cast<u32>(e);
+    nc += __popc(b);
+  }
+  __syncwarp();
+  if (qn > QSEG || nc > CT_CAP) {
+    if (lane == 0) sh.mode[s] = 1;
+    return;
+  }
+  const float bar_x = bar ? unord_f32(bar) : -INFINITY;
+  const int sv1 = sh.seg_v1[s];
+  const char* row = reinterpret_cast<const char*>(a.logits) + static_cast<int64_t>(sh.seg_r[s]) * a.ld * Elem<T>::BYTES;
+  for (int t = lane; t < nc; t += 32) {
+    const u32 vb = sh.ctile[s][t];
 #pragma unroll
-  for (int u = 0; u < BS_U; ++u) {
-    if (!(okmask & (1u << u))) continue;
-    float x[VEC];
-    if constexpr (VEC == 1) x[0] = __uint_as_float(qs[u].x);
-    else Vec16<T>::unpack(qs[u], x);
-    const u32 vu = vb + static_cast<u32>(u * BS_NC * VEC);
+    for (int u = 0; u < BS_U; ++u) {
+      const u32 v0 = vb + static_cast<u32>(u * BS_NC * VEC);
+      if (v0 >= static_cast<u32>(sv1)) continue;
+      float x[VEC];
+      if constexpr (VEC == 1) {
+        x[0] = Elem<T>::load(row, v0);
+      } else {
+        Vec16<T>::unpack(ld_stream16(row + static_cast<int64_t>(v0) * Elem<T>::BYTES), x);
+      }
 #pragma unroll
-    for (int e2 = 0; e2 < VEC; ++e2) {
-      if (x[e2] >= thr_x) {
-        const u64 k = make_key(x[e2], vu + e2);
-        if (k >= thr) crossed |= queue_push(sh, k);
+      for (int e2 = 0; e2 < VEC; ++e2) {
+        if (x[e2] >= bar_x) {
+          const int p = atomicAdd(&sh.fcnt[s], 1);
+          if (p < FIN_CAP) sh.fin[s][p] = make_key(x[e2], v0 + e2);
+        }
       }
     }
   }
-  return crossed;
+  __syncwarp();
+  if (lane == 0) sh.mode[s] = sh.fcnt[s] > FIN_CAP ? 1 : 0;
 }
 
-// The consumers: every chunk of the range, one row segment after the other.
+// All consumers, for a segment resolve_tiles could not finish: collect every key of the
+// segment at or above a bar, re-reading the segment from global memory, until one pass
+// fits in the queue; each pass that overflows raises the bar to the K-th best key it
+// queued (keys are distinct and QSEG > K, so the bar rises and the passes end).  Only
+// ties at the bar and adversarial orders (e.g. ascending logits) get here.
+template <typename T>
+__device__ void rescan_segment(const BsArgs& a, BsShared& sh, int s) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int K = a.K;
+  const int r = sh.seg_r[s], sv0 = sh.seg_v0[s], sv1 = sh.seg_v1[s];
+  const char* row = reinterpret_cast<const char*>(a.logits) + static_cast<int64_t>(r) * a.ld * Elem<T>::BYTES;
+  if (tid == 0) sh.rbar[s] = static_cast<u64>(sh.sbar[s]) << 32;
+  for (;;) {
+    named_sync(BAR_CONSUMERS, BS_NC);
+    const u64 bar = sh.rbar[s];
+    for (int i = tid; i < QSEG; i += BS_NC) sh.q[s][i] = 0ull;
+    if (tid == 0) sh.qcnt[s] = 0;
+    named_sync(BAR_CONSUMERS, BS_NC);
+    for (int v = sv0 + tid; v < sv1; v += BS_NC) {
+      const u64 k = make_key(Elem<T>::load(row, v), static_cast<u32>(v));
+      if (k >= bar) {
+        const int pos = atomicAdd(&sh.qcnt[s], 1);
+        if (pos < QSEG) sh.q[s][pos] = k;
+      }
+    }
+    named_sync(BAR_CONSUMERS, BS_NC);
+    if (sh.qcnt[s] <= QSEG) break;
+    if (warp == 0) {
+      warp_select_topk(sh.q[s], QSEG, K, sh.fin[s], lane);
+      if (lane == 0) sh.rbar[s] = sh.fin[s][K - 1];
+    }
+  }
+  if (tid == 0) sh.mode[s] = 2;
+  named_sync(BAR_CONSUMERS, BS_NC);
+}
+
+// One warp: segment s's partial -- (max, scaled sum) over the warps and its K best keys,
+// sorted -- written to its slot of the row's partials; then the slot is cleared.
+__device__ void finish_segment(const BsArgs& a, BsShared& sh, int s, int lane) {
+  const int K = a.K;
+  const int mode = sh.mode[s];
+  if (!sh.seg_skip[s]) {
+    float Mw = lane < BS_NCW ? sh.M[s][lane] : -INFINITY;
+    float lw = lane < BS_NCW ? sh.l[s][lane] : 0.f;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float M2 = __shfl_xor_sync(FULL, Mw, off);
+      const float l2 = __shfl_xor_sync(FULL, lw, off);
+      lse_merge(Mw, lw, M2, l2);
+    }
+    const int r = sh.seg_r[s];
+    const int64_t pslot = static_cast<int64_t>(r) * a.P + (static_cast<int>(blockIdx.x) - a.row_p0[r]);
+    u64* out = a.part_key + pslot * K;
+    if (mode == 0) {
+      const int cnt = sh.fcnt[s];
+      for (int j = lane; j < cnt; j += 32) {
+        const u64 k = sh.fin[s][j];
+        int rank = 0;
+        for (int i = 0; i < cnt; ++i) rank += sh.fin[s][i] > k;
+        if (rank < K) out[rank] = k;
+      }
+      if (lane < K && lane >= cnt) out[lane] = 0ull;
+    } else {
+      warp_select_topk(sh.q[s], min(sh.qcnt[s], QSEG), K, sh.fin[s], lane);
+      if (lane < K) out[lane] = sh.fin[s][lane];
+    }
+    if (lane == 0) { a.part_M[pslot] = Mw; a.part_l[pslot] = lw; }
+  }
+  __syncwarp();
+  const int n = mode == 0 ? min(sh.qcnt[s], QSEG) : QSEG;
+  for (int j = lane; j < n; j += 32) sh.q[s][j] = 0ull;
+  if (lane == 0) { sh.qcnt[s] = 0; sh.qref[s] = 0; sh.thr[s] = 0u; sh.mode[s] = 0; }
+}
+
+// All consumers (after a consumer barrier): publish slots [0, ns).
+template <typename T, int VEC>
+__device__ void publish_slots(const BsArgs& a, BsShared& sh, int ns) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (warp < ns && !sh.seg_skip[warp]) resolve_tiles<T, VEC>(a, sh, warp, lane);
+  named_sync(BAR_CONSUMERS, BS_NC);
+  for (int s = 0; s < ns; ++s)
+    if (!sh.seg_skip[s] && sh.mode[s] == 1) rescan_segment<T>(a, sh, s);
+  if (warp < ns) finish_segment(a, sh, warp, lane);
+}
+
+// The consumers: every chunk of the range, one row segment after the other.  Nothing in
+// the loop waits for another warp; segments are published after the loop (or when all
+// NSLOT slots hold one).
 template <typename T, bool TMA>
 __device__ void consume(const BsArgs& a, BsShared& sh, int64_t e0, int64_t e1) {
   constexpr int VEC = TMA ? Vec16<T>::N : 1;
   constexpr int64_t SE = static_cast<int64_t>(BS_NC) * BS_U * VEC;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K = a.K;
-  u64 thr = 0;
   float M = -INFINITY, m = -INFINITY, l = 0.f;
-  bool skip = false;
-  int seg_v0 = 0;
+  bool skip = false, seeded = false;
+  int seg = -1, slot = 0;
   ChunkCursor cur(e0, e1, a.V, static_cast<int>(SE));
   for (int c = 0; cur.more(); ++c) {
     const Chunk ch = cur.next();
     if (ch.first) {
+      ++seg;
+      slot = seg % NSLOT;
+      if (seg > 0 && slot == 0) {                   // every slot holds a segment: publish them
+        named_sync(BAR_CONSUMERS, BS_NC);
+        publish_slots<T, VEC>(a, sh, NSLOT);
+        named_sync(BAR_CONSUMERS, BS_NC);
+      }
       skip = row_skipped(a, ch.r);
-      seg_v0 = ch.v0;
-      thr = 0;
+      if (tid == 0) { sh.seg_r[slot] = ch.r; sh.seg_v0[slot] = ch.v0; sh.seg_skip[slot] = skip ? 1 : 0; }
       M = -INFINITY;
       m = -INFINITY;
       l = 0.f;
+      seeded = false;
     }
     const int n = ch.len / VEC;                     // vectors in this chunk
     uint4 q[BS_U];
     float xs[BS_U];
-    bool ok[BS_U];
     if constexpr (TMA) {
-      const int slot = c % NSTAGE;
-      if (!mbar_wait(&sh.full[slot], static_cast<u32>((c / NSTAGE) & 1))) set_status(a.status, VBS_ETIMEOUT);
+      const int rs = c % NSTAGE;
+      if (!mbar_wait(&sh.full[rs], static_cast<u32>((c / NSTAGE) & 1))) set_status(a.status, VBS_ETIMEOUT);
 #pragma unroll
       for (int u = 0; u < BS_U; ++u) {
         const int i = tid + u * BS_NC;
-        ok[u] = !skip && i < n;
         constexpr u32 NEG = VecMax<T>::NEG;
-        q[u] = ok[u] ? *reinterpret_cast<const uint4*>(sh.ring[slot] + i * 16) : make_uint4(NEG, NEG, NEG, NEG);
+        q[u] = (!skip && i < n) ? *reinterpret_cast<const uint4*>(sh.ring[rs] + i * 16) : make_uint4(NEG, NEG, NEG, NEG);
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.empty[slot]);  // the slot may refill once every warp has its data
+      if (lane == 0) mbar_arrive(&sh.empty[rs]);    // the stage may refill once every warp has its data
     } else {
       const char* row = reinterpret_cast<const char*>(a.logits) +
                         (static_cast<int64_t>(ch.r) * a.ld + ch.v0) * Elem<T>::BYTES;
 #pragma unroll
       for (int u = 0; u < BS_U; ++u) {
         const int i = tid + u * BS_NC;
-        ok[u] = !skip && i < n;
-        xs[u] = ok[u] ? Elem<T>::load(row, i) : -INFINITY;
+        xs[u] = (!skip && i < n) ? Elem<T>::load(row, i) : -INFINITY;
       }
     }
     if (!skip) {
@@ -389,92 +496,42 @@ __device__ void consume(const BsArgs& a, BsShared& sh, int64_t e0, int64_t e1) {
           for (int u = 0; u + w < BS_U; u += 2 * w) acc[u] += acc[u + w];
         l += acc[0];
       }
-      if (ch.first) {
-        // the threshold seed: each warp offers its kw best first-tile lower bounds; the
-        // K-th best of that pool is a lower bound of the segment's K-th best
-        int ulast = -1;
-#pragma unroll
-        for (int u = 0; u < BS_U; ++u) ulast = ok[u] ? u : ulast;
-        const u64 lb = ulast >= 0 ? make_key(tm, static_cast<u32>(ch.v0 + (tid + ulast * BS_NC) * VEC + VEC - 1))
-                                  : 0ull;
-        const int kw = max(2, (2 * K + BS_NCW - 1) / BS_NCW);
-        sh.lbk[tid] = lb;
-        for (int i = tid; i < QCAP; i += BS_NC) sh.q[i] = 0ull;
-        if (tid == 0) { sh.qcnt = 0; sh.ovf = 0; }
-        if (lane < kw) sh.pool[warp * kw + lane] = 0ull;
-        __syncwarp();
-        int rk = 0;
-        for (int q2 = 0; q2 < 32; ++q2) rk += sh.lbk[warp * 32 + q2] > lb;
-        if (lb != 0 && rk < kw) sh.pool[warp * kw + rk] = lb;
-        named_sync(BAR_CONSUMERS, BS_NC);
-        if (warp == 0) {
-          const int np = BS_NCW * kw;
-          u64 mine = 0;
-          for (int j = lane; j < np; j += 32) {
-            const u64 k = sh.pool[j];
-            int rank = 0;
-            for (int q2 = 0; q2 < np; ++q2) rank += sh.pool[q2] > k;
-            if (k != 0 && rank == K - 1) mine = k;
-          }
-          const u64 seed = warp_max_u64(mine);      // 0 when fewer than K lower bounds exist
-          if (lane == 0) sh.thr = seed;
-        }
-        named_sync(BAR_CONSUMERS, BS_NC);
-        thr = sh.thr;
-      } else {
-        const u64 t2 = *reinterpret_cast<volatile u64*>(&sh.thr);
-        thr = t2 > thr ? t2 : thr;
-      }
-      // candidates: only lanes whose tile can beat the threshold, one queue push per key
-      const float thr_x = thr ? key_x(thr) : -INFINITY;
-      bool crossed = false;
-      if (tm >= thr_x && tm > -INFINITY) {
-        u32 okmask = 0;
-#pragma unroll
-        for (int u = 0; u < BS_U; ++u) okmask |= ok[u] ? 1u << u : 0u;
-        const u32 vb = static_cast<u32>(ch.v0 + tid * VEC);
-        if constexpr (TMA) {
-          crossed = push_tile<T, VEC>(sh, q[0], q[1], q[2], q[3], okmask, vb, thr_x, thr);
-        } else {
-          crossed = push_tile<T, 1>(sh, make_uint4(__float_as_uint(xs[0]), 0, 0, 0),
-                                    make_uint4(__float_as_uint(xs[1]), 0, 0, 0),
-                                    make_uint4(__float_as_uint(xs[2]), 0, 0, 0),
-                                    make_uint4(__float_as_uint(xs[3]), 0, 0, 0), okmask, vb, thr_x, thr);
+      // the threshold: each warp seeds it at the segment's first chunk with the K-th best
+      // of its lane maxima; one warp per chunk raises it from the queue once QSTEP more
+      // tiles have been queued
+      u32 thr_o = *reinterpret_cast<volatile u32*>(&sh.thr[slot]);
+      const u32 tmo = tm > -INFINITY ? ord_f32(tm) : 0u;
+      if (!seeded) {
+        seeded = true;
+        const u32 seed = warp_kth_u32(tmo, K, lane);
+        if (seed > thr_o) {
+          if (lane == 0) atomicMax(&sh.thr[slot], seed);
+          thr_o = seed;
         }
       }
-      if (__any_sync(FULL, crossed)) queue_refresh(sh, K, lane);
+      if (tmo != 0u && tmo >= thr_o) {
+        const int pos = atomicAdd(&sh.qcnt[slot], 1);
+        if (pos < QSEG) sh.q[slot][pos] = (static_cast<u64>(tmo) << 32) | static_cast<u32>(ch.v0 + tid * VEC);
+      }
+      if (warp == (c & (BS_NCW - 1))) {
+        const int nq = __shfl_sync(FULL, *reinterpret_cast<volatile int*>(&sh.qcnt[slot]), 0);
+        const int nr = __shfl_sync(FULL, *reinterpret_cast<volatile int*>(&sh.qref[slot]), 0);
+        if (nq >= nr + QSTEP) queue_refresh(sh, slot, nq < QSEG ? nq : QSEG, K, lane);
+      }
     }
     if (ch.last) {
-      // ---- the segment's partial: (max, scaled sum, K sorted keys) ----
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) {
         const float M2 = __shfl_xor_sync(FULL, M, off);
         const float l2 = __shfl_xor_sync(FULL, l, off);
         lse_merge(M, l, M2, l2);
       }
-      if (lane == 0) { sh.M[warp] = M; sh.l[warp] = l; }
-      named_sync(BAR_CONSUMERS, BS_NC);
-      if (!skip && sh.ovf) rescan_segment<T>(a, sh, ch.r, seg_v0, static_cast<int64_t>(ch.v0) + ch.len);
-      if (warp == 0) {
-        float Mw = lane < BS_NCW ? sh.M[lane] : -INFINITY;
-        float lw = lane < BS_NCW ? sh.l[lane] : 0.f;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-          const float M2 = __shfl_xor_sync(FULL, Mw, off);
-          const float l2 = __shfl_xor_sync(FULL, lw, off);
-          lse_merge(Mw, lw, M2, l2);
-        }
-        const int nq = skip ? 0 : min(sh.qcnt, QCAP);
-        if (nq <= 128) warp_rank_topk(sh.q, nq, K, sh.ptop, lane);
-        else warp_select_topk(sh.q, nq, K, sh.ptop, lane);
-        const int pidx = static_cast<int>(blockIdx.x) - a.row_p0[ch.r];
-        const int64_t slot = static_cast<int64_t>(ch.r) * a.P + pidx;
-        if (lane < K) a.part_key[slot * K + lane] = sh.ptop[lane];
-        if (lane == 0) { a.part_M[slot] = Mw; a.part_l[slot] = lw; }
-      }
-      named_sync(BAR_CONSUMERS, BS_NC);
+      if (lane == 0) { sh.M[slot][warp] = M; sh.l[slot][warp] = l; }
+      if (tid == 0) sh.seg_v1[slot] = ch.v0 + ch.len;
     }
   }
+  named_sync(BAR_CONSUMERS, BS_NC);
+  if (seg >= 0) publish_slots<T, VEC>(a, sh, slot + 1);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -496,6 +553,13 @@ __global__ void __launch_bounds__(BS_NT, 1) bs_stream_kernel(const BsArgs a) {
       }
       fence_mbar_init();
     }
+    if (threadIdx.x < NSLOT) {
+      sh.thr[threadIdx.x] = 0u;
+      sh.qcnt[threadIdx.x] = 0;
+      sh.qref[threadIdx.x] = 0;
+      sh.mode[threadIdx.x] = 0;
+    }
+    for (int i = threadIdx.x; i < NSLOT * QSEG; i += BS_NT) (&sh.q[0][0])[i] = 0ull;
     __syncthreads();
     if ((threadIdx.x >> 5) == BS_NCW) {
       if constexpr (TMA) {
