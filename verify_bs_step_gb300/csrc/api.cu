@@ -225,6 +225,8 @@ VBS_EXPORT int bs_step(vbs_bs* c, const void* logits, int64_t ld, float* scores,
   a.lp_t = length_penalty(a.t, a.alpha, a.lp_kind);
   a.lp_bound = (a.early_stopping == VBS_ES_NEVER && a.alpha > 0.0) ? length_penalty(a.max_len, a.alpha, a.lp_kind)
                                                                    : a.lp_t;
+  a.lp_tf = static_cast<float>(a.lp_t);
+  a.lp_boundf = static_cast<float>(a.lp_bound);
   const int es = a.dtype == VBS_BF16 ? 2 : 4;
   const int VEC = 16 / es;
   const bool vec_ok = aligned16(logits) && (ld * es) % 16 == 0 && a.V % VEC == 0;

@@ -30,6 +30,7 @@ struct BsArgs {
   double alpha;
   double lp_t;                    // lp(t): normalises an EOS hit of this step (finalize: lp(steps run))
   double lp_bound;                // lp of the stopping test's best attainable length
+  float lp_tf, lp_boundf;         // the same two in fp32 (the walk and the stopping test run in fp32)
   // workspace
   float* part_M;
   float* part_l;

@@ -127,10 +127,13 @@ struct BsShared {                              // the stream kernel
   int fcnt[NSLOT];                             // keys found at the final bar
   int mode[NSLOT];                             // 0: tiles resolved, 1: needs a rescan, 2: q holds keys
   int seg_r[NSLOT], seg_v0[NSLOT], seg_v1[NSLOT], seg_skip[NSLOT];
+  int stage_skip[NSTAGE];                      // the producer's skip decision for each ring stage
 };
 
 struct MergeShared {                           // the merge kernel
   u64 rowscratch[WMAX * PART_KEYS];            // the rows' partial lists
+  float pM[PART_KEYS / 2], pL[PART_KEYS / 2];  // the rows' partial (max, sum): W * P <= PART_KEYS / 2
+  int np[WMAX];                                // partials per row
   u64 wtop[WMAX * KMAX];                       // the W rows' sorted lists
   float candv[WMAX * KMAX];                    // their candidate scores, list order
   int nval[WMAX];
@@ -138,10 +141,10 @@ struct MergeShared {                           // the merge kernel
   float sel_c[KMAX];
   int tile[SEQ_TILE_INTS];                     // the parents' sequence rows
   float s[WMAX];
-  double f_ns[WMAX];
+  float f_ns[WMAX];                            // normalised scores (all float-representable)
   int f_len[WMAX], f_serial[WMAX], f_src[WMAX];
   int f_count, f_next;
-  double f_worst;
+  float f_worst;
   float nb_score[WMAX];
   int nb_tok[WMAX], nb_row[WMAX];
   int done_now;
@@ -255,6 +258,7 @@ __device__ void produce(const BsArgs& a, BsShared& sh, int64_t e0, int64_t e1) {
     if (c >= NSTAGE && !mbar_wait(&sh.empty[slot], static_cast<u32>(((c / NSTAGE) + 1) & 1)))
       set_status(a.status, VBS_ETIMEOUT);
     const u32 bytes = skip ? 0u : static_cast<u32>(ch.len * Elem<T>::BYTES);
+    sh.stage_skip[slot] = skip ? 1 : 0;               // published by the arrive below
     mbar_expect_tx(&sh.full[slot], bytes);
     if (bytes) {
       const char* src = reinterpret_cast<const char*>(a.logits) +
@@ -426,8 +430,7 @@ __device__ void consume(const BsArgs& a, BsShared& sh, int64_t e0, int64_t e1) {
         publish_slots<T, VEC>(a, sh, NSLOT);
         named_sync(BAR_CONSUMERS, BS_NC);
       }
-      skip = row_skipped(a, ch.r);
-      if (tid == 0) { sh.seg_r[slot] = ch.r; sh.seg_v0[slot] = ch.v0; sh.seg_skip[slot] = skip ? 1 : 0; }
+      if constexpr (!TMA) skip = row_skipped(a, ch.r);
       M = -INFINITY;
       m = -INFINITY;
       l = 0.f;
@@ -439,6 +442,7 @@ __device__ void consume(const BsArgs& a, BsShared& sh, int64_t e0, int64_t e1) {
     if constexpr (TMA) {
       const int rs = c % NSTAGE;
       if (!mbar_wait(&sh.full[rs], static_cast<u32>((c / NSTAGE) & 1))) set_status(a.status, VBS_ETIMEOUT);
+      skip = sh.stage_skip[rs] != 0;                // the producer's decision for this row
 #pragma unroll
       for (int u = 0; u < BS_U; ++u) {
         const int i = tid + u * BS_NC;
@@ -455,6 +459,11 @@ __device__ void consume(const BsArgs& a, BsShared& sh, int64_t e0, int64_t e1) {
         const int i = tid + u * BS_NC;
         xs[u] = (!skip && i < n) ? Elem<T>::load(row, i) : -INFINITY;
       }
+    }
+    if (ch.first && tid == 0) {
+      sh.seg_r[slot] = ch.r;
+      sh.seg_v0[slot] = ch.v0;
+      sh.seg_skip[slot] = skip ? 1 : 0;
     }
     if (!skip) {
       float tm;
@@ -577,10 +586,41 @@ __global__ void __launch_bounds__(BS_NT, 1) bs_stream_kernel(const BsArgs a) {
 // the merge kernel: one CTA per sentence
 // ---------------------------------------------------------------------------------------
 
-// Warp-wide: row r's LSE (split hi + lo in fp32) and its sorted top-K list with scores.
-__device__ void row_merge(const BsArgs& a, MergeShared& sm, int r, int w, int lane) {
+// All threads: one round of independent loads of sentence b's rows' partial slots (all P
+// of them; the merge uses the first np).  P * K <= PART_KEYS and W * P <= PART_KEYS / 2.
+__device__ void merge_prefetch_partials(const BsArgs& a, MergeShared& sm, int b, int nthreads) {
+  const int W = a.W, K = a.K, P = a.P;
+  const int r0 = b * W;
+  const int PK = P * K;
+  const u64* keys = a.part_key + static_cast<int64_t>(r0) * PK;
+  for (int f = threadIdx.x; f < W * PK; f += nthreads) {
+    const int w = f / PK;
+    sm.rowscratch[w * PART_KEYS + (f - w * PK)] = __ldcg(keys + f);
+  }
+  for (int f = threadIdx.x; f < W * P; f += nthreads) {
+    sm.pM[f] = __ldcg(a.part_M + static_cast<int64_t>(r0) * P + f);
+    sm.pL[f] = __ldcg(a.part_l + static_cast<int64_t>(r0) * P + f);
+  }
+}
+
+// Sentence b's rows' scores and partial counts (neither is written by the stream kernel).
+__device__ void merge_prefetch_rows(const BsArgs& a, MergeShared& sm, int b) {
+  const int r0 = b * a.W;
+  if (threadIdx.x < a.W) {
+    sm.s[threadIdx.x] = __ldcg(a.scores + r0 + threadIdx.x);
+    sm.np[threadIdx.x] = a.row_np[r0 + threadIdx.x];
+  }
+}
+
+// fp32 ln 2 split in two: LN2_HI = fl(ln 2), LN2_LO = ln 2 - LN2_HI.
+constexpr float LN2_HI = 0.693147182464599609375f;
+constexpr float LN2_LO = -1.904654299957768e-09f;
+
+// Warp-wide, from the prefetched partials: row w's LSE (split hi + lo in fp32) and its
+// sorted top-K list with scores.
+__device__ void row_merge(const BsArgs& a, MergeShared& sm, int w, int lane) {
   const int K = a.K;
-  const float s = __ldcg(a.scores + r);
+  const float s = sm.s[w];
   if (s == -INFINITY) {
     // every candidate of the row is -inf: they rank by token id
     const int nv = K < a.V ? K : a.V;
@@ -591,25 +631,35 @@ __device__ void row_merge(const BsArgs& a, MergeShared& sm, int r, int w, int la
     if (lane == 0) sm.nval[w] = nv;
     return;
   }
-  const int n = a.row_np[r];
-  const int64_t base = static_cast<int64_t>(r) * a.P;
-  u64* scratch = sm.rowscratch + w * PART_KEYS;
-  for (int c = lane; c < n * K; c += 32) scratch[c] = __ldcg(a.part_key + base * K + c);
+  const int n = sm.np[w];
+  const u64* scratch = sm.rowscratch + w * PART_KEYS;
   float Mc = -INFINITY, lc = 0.f;
-  for (int c = lane; c < n; c += 32) lse_merge(Mc, lc, __ldcg(a.part_M + base + c), __ldcg(a.part_l + base + c));
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
+  for (int c = lane; c < n; c += 32) lse_merge(Mc, lc, sm.pM[w * a.P + c], sm.pL[w * a.P + c]);
+  for (int off = 1; off < n && off < 32; off <<= 1) {      // lanes >= n hold (-inf, 0)
     const float M2 = __shfl_xor_sync(FULL, Mc, off);
     const float l2 = __shfl_xor_sync(FULL, lc, off);
     lse_merge(Mc, lc, M2, l2);
   }
-  __syncwarp();
+  Mc = __shfl_sync(FULL, Mc, 0);
+  lc = __shfl_sync(FULL, lc, 0);
   u64* out = sm.wtop + w * K;
-  warp_merge_sorted(scratch, n, K, out, lane);
-  const double lse = LN2_D * (static_cast<double>(Mc) + static_cast<double>(log2f(lc)));
-  const float hi = static_cast<float>(lse);
-  const float lo = static_cast<float>(lse - static_cast<double>(hi));
-  if (lane == 0 && !(lse > -INFINITY && lse < INFINITY)) set_status(a.status, VBS_EINPUT);  // no finite logit, NaN, +inf
+  if (n == 1) {
+    if (lane < K) out[lane] = scratch[lane];
+    __syncwarp();
+  } else {
+    warp_merge_sorted(scratch, n, K, out, lane);
+  }
+  // LSE = ln2 * (Mc + log2 lc) as an unevaluated fp32 sum hi + lo (error-free sum and
+  // product steps; FP64 is slow on this part and not needed)
+  const float L2 = log2f(lc);
+  const float t_hi = Mc + L2;
+  const float bb = t_hi - Mc;
+  const float t_lo = (Mc - (t_hi - bb)) + (L2 - bb);
+  const float p = t_hi * LN2_HI;
+  const float e = fmaf(t_hi, LN2_HI, -p) + fmaf(t_hi, LN2_LO, t_lo * LN2_HI);
+  const float hi = p + e;
+  const float lo = e - (hi - p);
+  if (lane == 0 && !(hi > -INFINITY && hi < INFINITY)) set_status(a.status, VBS_EINPUT);  // no finite logit, NaN, +inf
   if (lane < K) {
     const u64 k = out[lane];
     const float x = key_x(k);
@@ -644,33 +694,49 @@ __global__ void __launch_bounds__(MG_NT) bs_merge_kernel(const BsArgs a) {
   const int TW = SEQ_TILE_INTS / W;            // columns per row in one gather tile
   const int nc0 = min(t, TW);
 
-  // everything below reads what the stream kernel wrote
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const bool was_done = a.done[b] != 0;
-
-  if (!was_done) {
-    // the first gather tile and the sentence state load while the rows merge
-    for (int i = tid; i < W * nc0; i += MG_NT) {
-      const int w = i / nc0, c = i - w * nc0;
-      sm.tile[w * TW + c] = a.seqs[static_cast<int64_t>(r0 + w) * ld + c];
-    }
-    if (tid < W) {
-      sm.s[tid] = a.scores[r0 + tid];
-      sm.f_ns[tid] = a.fin_ns[r0 + tid];
-      sm.f_len[tid] = a.fin_len[r0 + tid];
-      sm.f_serial[tid] = a.fin_serial[r0 + tid];
-      sm.f_src[tid] = -1;
-    }
-    if (tid == 0) {
-      sm.f_count = a.fin_count[b];
-      sm.f_next = a.fin_next[b];
-      sm.f_worst = a.fin_worst[b];
-    }
-    for (int w = warp; w < W; w += MG_NW) row_merge(a, sm, r0 + w, w, lane);
+  // The stream kernel writes only the partials.  It starts after every earlier kernel on
+  // the stream has finished, so the sentence state, scores and sequences can load while
+  // it runs; the partials load after griddepcontrol.wait.
+  const int done_b = __ldcg(a.done + b);
+  merge_prefetch_rows(a, sm, b);
+  for (int i = tid; i < W * nc0; i += MG_NT) {
+    const int w = i / nc0, c = i - w * nc0;
+    sm.tile[w * TW + c] = a.seqs[static_cast<int64_t>(r0 + w) * ld + c];
   }
+  if (tid < W) {
+    sm.f_ns[tid] = static_cast<float>(a.fin_ns[r0 + tid]);
+    sm.f_len[tid] = a.fin_len[r0 + tid];
+    sm.f_serial[tid] = a.fin_serial[r0 + tid];
+    sm.f_src[tid] = -1;
+  }
+  if (tid == 0) {
+    sm.f_count = a.fin_count[b];
+    sm.f_next = a.fin_next[b];
+    sm.f_worst = static_cast<float>(a.fin_worst[b]);
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  merge_prefetch_partials(a, sm, b, MG_NT);
+  __syncthreads();
+  const bool was_done = done_b != 0;
+  if (!was_done)
+    for (int w = warp; w < W; w += MG_NW) row_merge(a, sm, w, lane);
   __syncthreads();
 
-  if (!was_done) {
+  if (!was_done && W * K <= 32) {
+    // one warp ranks every candidate by (score desc, flat index asc): list position f =
+    // w*K + i grows with the flat index, and invalid entries (0) rank last
+    if (warp == 0) {
+      const int w = lane / K, i = lane - w * K;
+      const bool valid = lane < W * K && i < sm.nval[w];
+      const float c = valid ? sm.candv[lane] : -INFINITY;
+      const int rank = warp_rank_u32(valid ? ord_f32(c) : 0u, lane);
+      if (valid && rank < 2 * W) {
+        sm.sel_w[rank] = w;
+        sm.sel_i[rank] = i;
+        sm.sel_c[rank] = c;
+      }
+    }
+  } else if (!was_done) {
     // rank every candidate of the W lists; the best 2W land in order
     for (int f = tid; f < W * K; f += MG_NT) {
       const int w = f / K, i = f - w * K;
@@ -688,55 +754,67 @@ __global__ void __launch_bounds__(MG_NT) bs_merge_kernel(const BsArgs a) {
   }
   __syncthreads();
 
-  if (tid == 0 && !was_done) {
-    // the walk of the ranked candidates
-    int new_cnt = 0;
-    const float lp_t = static_cast<float>(a.lp_t);
-    for (int rank = 0; rank < 2 * W && new_cnt < W; ++rank) {
-      const int w = sm.sel_w[rank];
-      const float c = sm.sel_c[rank];
-      const u32 v = key_v(sm.wtop[w * K + sm.sel_i[rank]]);
-      const int parent = r0 + w;
-      if (a.eos >= 0 && static_cast<int>(v) == a.eos) {
-        if (rank < W) {
-          // BeamHypotheses.add(hyp = the parent's sequence, sum = c), |y| = t
-          const double ns = static_cast<double>(c / lp_t);
-          int slot = -1;
-          if (sm.f_count < W) {
-            slot = sm.f_count++;
-            sm.f_worst = fmin(ns, sm.f_worst);
-          } else if (ns > sm.f_worst) {
-            slot = 0;                          // evict the worst; ties: the earliest inserted
-            for (int q = 1; q < W; ++q)
-              if (sm.f_ns[q] < sm.f_ns[slot] || (sm.f_ns[q] == sm.f_ns[slot] && sm.f_serial[q] < sm.f_serial[slot]))
-                slot = q;
-          }
-          if (slot >= 0) {
-            sm.f_ns[slot] = ns;
-            sm.f_len[slot] = t;
-            sm.f_serial[slot] = sm.f_next++;
-            sm.f_src[slot] = parent;
-            if (sm.f_count >= W) {
-              double wmin = sm.f_ns[0];
-              for (int q = 1; q < W; ++q) wmin = fmin(wmin, sm.f_ns[q]);
-              sm.f_worst = wmin;
-            }
+  if (warp == 0 && !was_done) {
+    // The walk of the ranked candidates, one lane per rank (2W <= 32): the k-th candidate
+    // that is not an EOS hit becomes new beam k, for k < W; an EOS hit at rank < W that
+    // the walk reaches (fewer than W live candidates before it) joins the finished set,
+    // in rank order.
+    int nv = lane < W ? sm.nval[lane] : 0;
+    nv = __reduce_add_sync(FULL, nv);
+    const bool have = lane < 2 * W && lane < nv;
+    int w = 0;
+    float c = -INFINITY;
+    u32 v = 0;
+    if (have) {
+      w = sm.sel_w[lane];
+      c = sm.sel_c[lane];
+      v = key_v(sm.wtop[w * K + sm.sel_i[lane]]);
+    }
+    const bool eos = have && a.eos >= 0 && v == static_cast<u32>(a.eos);
+    const u32 live = __ballot_sync(FULL, have && !eos);
+    const int before = __popc(live & ((1u << lane) - 1u));
+    if (have && !eos && before < W) {
+      sm.nb_score[before] = c;
+      sm.nb_tok[before] = static_cast<int>(v);
+      sm.nb_row[before] = r0 + w;
+    }
+    const u32 hits = __ballot_sync(FULL, eos && lane < W && before < W);
+    const int new_cnt = min(__popc(live), W);
+    if (lane == 0) {
+      const float lp_t = a.lp_tf;
+      for (u32 m = hits; m; m &= m - 1) {
+        const int rank = __ffs(m) - 1;
+        // BeamHypotheses.add(hyp = the parent's sequence, sum = c), |y| = t
+        const float ns = sm.sel_c[rank] / lp_t;
+        int slot = -1;
+        if (sm.f_count < W) {
+          slot = sm.f_count++;
+          sm.f_worst = fminf(ns, sm.f_worst);
+        } else if (ns > sm.f_worst) {
+          slot = 0;                            // evict the worst; ties: the earliest inserted
+          for (int q = 1; q < W; ++q)
+            if (sm.f_ns[q] < sm.f_ns[slot] || (sm.f_ns[q] == sm.f_ns[slot] && sm.f_serial[q] < sm.f_serial[slot]))
+              slot = q;
+        }
+        if (slot >= 0) {
+          sm.f_ns[slot] = ns;
+          sm.f_len[slot] = t;
+          sm.f_serial[slot] = sm.f_next++;
+          sm.f_src[slot] = r0 + sm.sel_w[rank];
+          if (sm.f_count >= W) {
+            float wmin = sm.f_ns[0];
+            for (int q = 1; q < W; ++q) wmin = fminf(wmin, sm.f_ns[q]);
+            sm.f_worst = wmin;
           }
         }
-      } else {
-        sm.nb_score[new_cnt] = c;
-        sm.nb_tok[new_cnt] = static_cast<int>(v);
-        sm.nb_row[new_cnt] = parent;
-        ++new_cnt;
       }
+      if (new_cnt < W) set_status(a.status, VBS_EINPUT);
+      for (int q = new_cnt; q < W; ++q) { sm.nb_score[q] = -INFINITY; sm.nb_tok[q] = a.pad; sm.nb_row[q] = r0; }
+      bool done = false;
+      if (sm.f_count >= W)
+        done = a.early_stopping == VBS_ES_TRUE || sm.f_worst >= sm.sel_c[0] / a.lp_boundf;
+      sm.done_now = done ? 1 : 0;
     }
-    if (new_cnt < W) set_status(a.status, VBS_EINPUT);
-    for (int q = new_cnt; q < W; ++q) { sm.nb_score[q] = -INFINITY; sm.nb_tok[q] = a.pad; sm.nb_row[q] = r0; }
-    bool done = false;
-    if (sm.f_count >= W)
-      done = a.early_stopping == VBS_ES_TRUE ||
-             sm.f_worst >= static_cast<double>(sm.sel_c[0]) / a.lp_bound;
-    sm.done_now = done ? 1 : 0;
   }
   if (tid == 0 && was_done) sm.done_now = 1;
   __syncthreads();
@@ -757,14 +835,14 @@ __global__ void __launch_bounds__(MG_NT) bs_merge_kernel(const BsArgs a) {
       a.beam_idx[r0 + tid] = sm.nb_row[tid];
       a.tokens[r0 + tid] = sm.nb_tok[tid];
       a.scores[r0 + tid] = sm.nb_score[tid];
-      a.fin_ns[r0 + tid] = sm.f_ns[tid];
+      a.fin_ns[r0 + tid] = static_cast<double>(sm.f_ns[tid]);
       a.fin_len[r0 + tid] = sm.f_len[tid];
       a.fin_serial[r0 + tid] = sm.f_serial[tid];
     }
     if (tid == 0) {
       a.fin_count[b] = sm.f_count;
       a.fin_next[b] = sm.f_next;
-      a.fin_worst[b] = sm.f_worst;
+      a.fin_worst[b] = static_cast<double>(sm.f_worst);
       a.done[b] = sm.done_now;
     }
     // sequences: gather the parents' columns [0, t) in place (tile 0 is prefetched), append the token
@@ -984,7 +1062,10 @@ __global__ void __launch_bounds__(MG_NT) bs_expand_merge_kernel(const BsArgs a, 
   const int W = a.W, K = a.K;
   const int r0 = blockIdx.x * W;
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  for (int w = warp; w < W; w += MG_NW) row_merge(a, sm, r0 + w, w, lane);
+  merge_prefetch_rows(a, sm, blockIdx.x);
+  merge_prefetch_partials(a, sm, blockIdx.x, MG_NT);
+  __syncthreads();
+  for (int w = warp; w < W; w += MG_NW) row_merge(a, sm, w, lane);
   if (tid < W) { sm.sel_w[tid] = 0; sm.sel_i[tid] = 0; sm.sel_c[tid] = -INFINITY; }
   __syncthreads();
   for (int f = tid; f < W * K; f += MG_NT) {
