@@ -8,12 +8,15 @@ Sentences the oracle does not check keep salt 0 and are generated on the
 device.  No value computed by the CUDA path ever feeds the oracle.
 
 Score tolerance, derived from the arithmetic: the kernel forms each candidate
-in fp64 from the fp32 cumulative score, the fp32 logit and a row LSE whose
-fp32 partial sums carry a relative error of about 1e-6, then rounds the new
-score to fp32 (half an ulp, 6e-8 |s|).  Over t steps the score therefore
-drifts by at most sum_i (6e-8 |s_i| + 2e-6) <= 3e-8 t |s_t| + 2e-6 t.  The test
-allows  |gpu - ref| <= 1e-5 |ref| + 4e-6 t  (the relative part holds the drift
-for t <= 300, the absolute part covers the LSE error with a factor 2).
+in fp32 as s + ((x - hi) - lo), from the fp32 cumulative score s, the exact
+logit x and the row LSE carried as an fp32 pair hi + lo; the LSE's fp32
+partial sums carry a relative error of about 1e-6 (about 1e-6 absolute at
+|LSE| ~ 10), the subtraction x - hi rounds by at most half an ulp of ~30
+(1e-6), and the new score rounds by half an ulp (6e-8 |s|).  Over t steps the
+score therefore drifts by at most sum_i (6e-8 |s_i| + 2e-6) <= 3e-8 t |s_t| +
+2e-6 t.  The test allows  |gpu - ref| <= 1e-5 |ref| + 4e-6 t  (the relative
+part holds the drift for t <= 300, the absolute part covers the per-step error
+with a factor 2).
 """
 
 from __future__ import annotations
