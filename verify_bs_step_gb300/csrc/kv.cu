@@ -324,14 +324,49 @@ struct CowMap {
   }
 };
 
-__global__ void __launch_bounds__(32) kv_cow_bulk_kernel(CowMap map, const int32_t* task_count, int32_t* cow_ticket,
-                                                         int32_t* task_count_rw, int* status) {
+// Copy-on-write items are short (one run's filled slots, a few KB) and scattered, so
+// the copy is warp-per-item with plain 16-byte vectors: each lane issues up to COW_U loads
+// before its stores, and 32 warps per SM keep about 128 KB in flight, which is what HBM
+// latency needs at full bandwidth.  The last CTA to finish clears the task list.
+constexpr int COW_NT = 256;
+constexpr int COW_CTAS_PER_SM = 4;
+constexpr int COW_U = 8;
+
+__device__ __forceinline__ void st_stream16(void* p, const uint4& v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+__global__ void __launch_bounds__(COW_NT) kv_cow_vec_kernel(CowMap map, int32_t* task_count, int32_t* cow_ticket) {
   const int64_t n_items = static_cast<int64_t>(*task_count) * map.n_runs;
-  bulk_copy_items(map, n_items, status);
+  const int lane = threadIdx.x & 31;
+  const int64_t nw = static_cast<int64_t>(gridDim.x) * (COW_NT / 32);
+  for (int64_t item = static_cast<int64_t>(blockIdx.x) * (COW_NT / 32) + (threadIdx.x >> 5); item < n_items;
+       item += nw) {
+    const char* src;
+    char* dst;
+    u32 bytes;
+    map(item, src, dst, bytes);
+    const int nv = static_cast<int>(bytes / 16);
+    for (int base = 0; base < nv; base += 32 * COW_U) {
+      uint4 v[COW_U];
+#pragma unroll
+      for (int u = 0; u < COW_U; ++u) {
+        const int i = base + u * 32 + lane;
+        if (i < nv) v[u] = ld_stream16(src + static_cast<int64_t>(i) * 16);
+      }
+#pragma unroll
+      for (int u = 0; u < COW_U; ++u) {
+        const int i = base + u * 32 + lane;
+        if (i < nv) st_stream16(dst + static_cast<int64_t>(i) * 16, v[u]);
+      }
+    }
+  }
+  __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
     if (atomicAdd(cow_ticket, 1) == static_cast<int>(gridDim.x) - 1) {
-      *task_count_rw = 0;
+      *task_count = 0;
       *cow_ticket = 0;
     }
   }
@@ -360,17 +395,10 @@ int launch_kv_paged_cow(const PagedArgs& a, bool bulk_ok, int num_sms, cudaStrea
   const int n_runs = a.L * 2 * a.H;
   const int64_t run_bytes = static_cast<int64_t>(a.block) * a.slot_bytes;
   CowMap m{a.pool, a.tasks, n_runs, a.block_bytes, run_bytes, a.slot_bytes};
-  const int grid = num_sms * KV_CTAS_PER_SM;
-  if (bulk_ok && run_bytes <= KV_CHUNK) {
-    const size_t smem = static_cast<size_t>(KV_STAGES) * KV_CHUNK;
-    static bool attr_set = false;
-    if (!attr_set) {
-      cudaFuncSetAttribute(kv_cow_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-      attr_set = true;
-    }
-    kv_cow_bulk_kernel<<<grid, 32, smem, s>>>(m, a.task_count, a.cow_ticket, a.task_count, a.status);
+  if (bulk_ok) {
+    kv_cow_vec_kernel<<<num_sms * COW_CTAS_PER_SM, COW_NT, 0, s>>>(m, a.task_count, a.cow_ticket);
   } else {
-    kv_cow_plain_kernel<<<grid, 256, 0, s>>>(m, a.task_count, a.cow_ticket);
+    kv_cow_plain_kernel<<<num_sms * KV_CTAS_PER_SM, 256, 0, s>>>(m, a.task_count, a.cow_ticket);
   }
   return cudaGetLastError() == cudaSuccess ? VBS_OK : VBS_ECUDA;
 }
