@@ -425,8 +425,13 @@ def run_e2e(args, torch, vbs, synth, dev, stream, ring, seed, world):
                     "beam_idx/tokens/scores copied back each step"}
 
 
-def _timed(torch, stream, fn, reps):
+def _timed(torch, stream, fn, reps, ahead=True):
+    """Event-bracketed calls; with `ahead`, the host queues them behind a GPU spin so that no
+    host launch gap lands between a call's events."""
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    torch.cuda.synchronize()
+    if ahead:
+        torch.cuda._sleep(int(2e5) * reps)
     for a, b in evs:
         a.record(stream)
         fn()
@@ -464,6 +469,7 @@ def run_extras(args, torch, vbs, synth, dev, stream, peak):
                 i += 1
                 evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                        for _ in range(T - 1)]
+                torch.cuda._sleep(int(2e5) * (T - 1))      # the host queues the decode ahead of the GPU
                 for e_a, e_b in evs:
                     e_a.record(stream)
                     L_.bs_step(bs.ctx, prs[i % n], V, *a_)

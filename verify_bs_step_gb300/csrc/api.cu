@@ -576,6 +576,8 @@ VBS_EXPORT int bpd_verify(const void* logits, const int32_t* proposals, int B, i
   if (eos >= V) return VBS_EINVAL;
   const int es = dtype == VBS_BF16 ? 2 : 4;
   const bool vec_ok = aligned16(logits) && (static_cast<int64_t>(V) * es) % 16 == 0;
-  return vbs::launch_bpd_verify(logits, proposals, B, k, V, dtype, vec_ok, eos, khat, next,
+  int* status = nullptr;
+  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_stateless_status) != cudaSuccess) return VBS_ECUDA;
+  return vbs::launch_bpd_verify(logits, proposals, B, k, V, dtype, vec_ok, eos, khat, next, status, num_sms(),
                                 reinterpret_cast<cudaStream_t>(stream));
 }

@@ -129,6 +129,189 @@ __global__ void __launch_bounds__(BPD_NT) bpd_verify_kernel(const void* logits, 
   }
 }
 
+// ---------------------------------------------------------------------------------------
+// the row argmax of one CTA (BPD_RT threads): each thread tracks the best vector of its
+// strided share with packed maxima (ties keep the earlier vector), then the first element
+// of that vector equal to its maximum; one reduction over (value, lower index)
+// ---------------------------------------------------------------------------------------
+
+constexpr int BPD_RT = 512;
+constexpr int BPD_BUF = 96 * 1024;        // shared staging of one row chunk (bulk copy)
+
+// The CTA's staging buffer and its mbarrier (one bulk copy in flight at a time).
+struct RowStage {
+  unsigned char* buf;
+  u64* bar;
+  u32 phase;
+};
+
+template <typename T, bool VECTOR>
+__device__ int row_argmax(const char* row, int V, RowStage& st, u64* red, int* status) {
+  constexpr int VEC = VECTOR ? Vec16<T>::N : 1;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  u64 best = 0;
+  if constexpr (VECTOR) {
+    // the row in chunks of at most BPD_BUF bytes: one bulk copy each, then a scan of the
+    // staged vectors from shared memory
+    const int nvec = V / VEC;
+    constexpr int CH = BPD_BUF / 16;
+    float bv = -INFINITY;
+    int bi = -1;
+    uint4 bq = make_uint4(0, 0, 0, 0);
+    for (int c0 = 0; c0 < nvec; c0 += CH) {
+      const int nv = min(CH, nvec - c0);
+      __syncthreads();                             // the buffer's previous contents are consumed
+      if (tid == 0) {
+        mbar_expect_tx(st.bar, static_cast<u32>(nv) * 16u);
+        bulk_g2s(st.buf, row + static_cast<int64_t>(c0) * 16, static_cast<u32>(nv) * 16u, st.bar);
+      }
+      if (!mbar_wait(st.bar, st.phase)) set_status(status, VBS_ETIMEOUT);
+      st.phase ^= 1u;
+      const uint4* v = reinterpret_cast<const uint4*>(st.buf);
+      for (int i = tid; i < nv; i += BPD_RT) {
+        const uint4 q = v[i];
+        const float m = VecMax<T>::finish(VecMax<T>::fold(q, VecMax<T>::NEG));
+        if (m > bv || bi < 0) { bv = m; bi = c0 + i; bq = q; }
+      }
+    }
+    if (bi >= 0) {
+      float x[VEC];
+      Vec16<T>::unpack(bq, x);
+      int e = VEC - 1;
+#pragma unroll
+      for (int e2 = VEC - 1; e2 >= 0; --e2) e = x[e2] == bv ? e2 : e;
+      best = make_key(bv, static_cast<u32>(bi * VEC + e));
+    }
+  } else {
+    for (int i = tid; i < V; i += BPD_RT) {
+      const u64 k = make_key(Elem<T>::load(row, i), static_cast<u32>(i));
+      best = k > best ? k : best;
+    }
+  }
+  best = warp_max_u64(best);
+  if (lane == 0) red[warp] = best;
+  __syncthreads();
+  if (warp == 0) {
+    u64 v = lane < BPD_RT / 32 ? red[lane] : 0ull;
+    v = warp_max_u64(v);
+    if (lane == 0) red[BPD_RT / 32] = v;
+  }
+  __syncthreads();
+  return static_cast<int>(key_v(red[BPD_RT / 32]));
+}
+
+// ---------------------------------------------------------------------------------------
+// verify + accept as a persistent work queue
+// ---------------------------------------------------------------------------------------
+//
+// Units, handed out in order by one atomic counter: unit b < B is b's verify chain (head
+// 0 at positions 0, 1, ... while the proposals agree, then head 0 at position khat-1 if
+// the chain did not read it); unit B + b*(k-1) + (h-1) is the row of head h at position
+// khat_b - 1, which waits for b's chain through a flag.  Every chain is handed out before
+// any row that waits for it, to a CTA that is already running, so no wait can block the
+// chain it waits for; waits are bounded all the same.  Only the rows the definition
+// needs are read.  The counters and flags are static device memory, reset by the last
+// CTA of each call (calls on one stream run one after the other).
+
+constexpr int BPD_MAX_B = 65536;
+__device__ unsigned g_bpd_flag[BPD_MAX_B];   // == epoch + 1 once b's chain is done
+__device__ unsigned g_bpd_epoch;
+__device__ int g_bpd_next_unit;
+__device__ int g_bpd_exited;
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+
+template <typename T, bool VECTOR>
+__global__ void __launch_bounds__(BPD_RT, 2) bpd_verify_queue_kernel(const void* logits, const int32_t* proposals, int B,
+                                                                  int k, int V, int eos, int32_t* khat_out,
+                                                                  int32_t* next_out, int* status) {
+  extern __shared__ __align__(128) unsigned char bpd_smem[];
+  __shared__ u64 red[BPD_RT / 32 + 1];
+  __shared__ __align__(8) u64 bar;
+  __shared__ int s_unit;
+  __shared__ int s_am[KMAX];
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  RowStage st{bpd_smem, &bar, 0u};
+  const unsigned epoch = *reinterpret_cast<volatile unsigned*>(&g_bpd_epoch);
+  const int64_t row_bytes = static_cast<int64_t>(V) * Elem<T>::BYTES;
+  const int total = B + B * (k - 1);
+  // the next unit is claimed while the current one is processed (its atomic's latency hidden)
+  int claimed = 0;
+  if (tid == 0) claimed = atomicAdd(&g_bpd_next_unit, 1);
+  for (;;) {
+    if (tid == 0) s_unit = claimed;
+    __syncthreads();
+    const int u = s_unit;
+    __syncthreads();
+    if (u >= total) break;
+    if (tid == 0) claimed = atomicAdd(&g_bpd_next_unit, 1);
+    if (u < B) {
+      // b's verify chain
+      const int b = u;
+      const char* base = reinterpret_cast<const char*>(logits) + static_cast<int64_t>(b) * k * k * row_bytes;
+      const int32_t* props = proposals + static_cast<int64_t>(b) * k;
+      int checks = k - 1;                          // proposals up to an EOS need no checks past it
+      if (eos >= 0)
+        for (int e = 0; e < k; ++e)
+          if (__ldg(props + e) == eos) { checks = min(checks, e); break; }
+      int n = 1, am = -1;
+      for (int p = 0; p < checks; ++p) {
+        am = row_argmax<T, VECTOR>(base + static_cast<int64_t>(p) * k * row_bytes, V, st, red, status);
+        if (__ldg(props + p + 1) != am) break;
+        ++n;
+      }
+      if (n - 1 == checks)                         // khat - 1 not read by the checks: head 0 there
+        am = row_argmax<T, VECTOR>(base + static_cast<int64_t>(n - 1) * k * row_bytes, V, st, red, status);
+      if (tid == 0) {
+        khat_out[b] = n;
+        next_out[static_cast<int64_t>(b) * k] = am;
+        st_release_u32(&g_bpd_flag[b], epoch + 1u);
+      }
+    } else {
+      // head h at position khat_b - 1
+      const int f = u - B;
+      const int b = f / (k - 1), h = f - b * (k - 1) + 1;
+      if (tid == 0) {
+        u32 it = 0;
+        while (ld_acquire_u32(&g_bpd_flag[b]) != epoch + 1u) {
+          if (++it > (1u << 24)) { set_status(status, VBS_ETIMEOUT); break; }
+          __nanosleep(64);
+        }
+        s_am[0] = *reinterpret_cast<volatile int32_t*>(khat_out + b);
+      }
+      __syncthreads();
+      const int q = max(1, min(s_am[0], k)) - 1;
+      __syncthreads();
+      const char* row = reinterpret_cast<const char*>(logits) +
+                        ((static_cast<int64_t>(b) * k + q) * k + h) * row_bytes;
+      const int am = row_argmax<T, VECTOR>(row, V, st, red, status);
+      if (tid == 0) next_out[static_cast<int64_t>(b) * k + h] = am;
+    }
+  }
+  // the last CTA out resets the queue and moves the flags to the next epoch
+  if (tid == 0) {
+    __threadfence();
+    if (atomicAdd(&g_bpd_exited, 1) == static_cast<int>(gridDim.x) - 1) {
+      g_bpd_next_unit = 0;
+      g_bpd_exited = 0;
+      __threadfence();
+      atomicAdd(&g_bpd_epoch, 1u);
+    }
+  }
+}
+
 template <typename T, bool VECTOR>
 __global__ void __launch_bounds__(256) bpd_propose_kernel(const void* logits, int V, int32_t* proposals) {
   constexpr int VEC = VECTOR ? Vec16<T>::N : 1;
@@ -161,9 +344,32 @@ int launch_bpd_propose(const void* logits, int B, int k, int V, int dtype, bool 
   return cudaGetLastError() == cudaSuccess ? VBS_OK : VBS_ECUDA;
 }
 
+template <typename T, bool VECTOR>
+static int launch_queue(int grid, const void* logits, const int32_t* proposals, int B, int k, int V, int eos,
+                        int32_t* khat, int32_t* next, int* status, cudaStream_t s) {
+  const int smem = VECTOR ? BPD_BUF : 0;
+  static bool attr_set = false;                  // one per kernel instantiation
+  if (VECTOR && !attr_set) {
+    if (cudaFuncSetAttribute(bpd_verify_queue_kernel<T, VECTOR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             BPD_BUF) != cudaSuccess)
+      return VBS_ECUDA;
+    attr_set = true;
+  }
+  bpd_verify_queue_kernel<T, VECTOR><<<grid, BPD_RT, smem, s>>>(logits, proposals, B, k, V, eos, khat, next, status);
+  return cudaGetLastError() == cudaSuccess ? VBS_OK : VBS_ECUDA;
+}
+
 int launch_bpd_verify(const void* logits, const int32_t* proposals, int B, int k, int V, int dtype, bool vec_ok,
-                      int eos, int32_t* khat, int32_t* next, cudaStream_t s) {
+                      int eos, int32_t* khat, int32_t* next, int* status, int num_sms, cudaStream_t s) {
   if (B == 0) return VBS_OK;
+  if (B <= BPD_MAX_B) {
+    const int grid = std::min(B * k, num_sms * 2);  // two CTAs (two staged rows) per SM
+    if (dtype == VBS_BF16)
+      return vec_ok ? launch_queue<bf16_t, true>(grid, logits, proposals, B, k, V, eos, khat, next, status, s)
+                    : launch_queue<bf16_t, false>(grid, logits, proposals, B, k, V, eos, khat, next, status, s);
+    return vec_ok ? launch_queue<float, true>(grid, logits, proposals, B, k, V, eos, khat, next, status, s)
+                  : launch_queue<float, false>(grid, logits, proposals, B, k, V, eos, khat, next, status, s);
+  }
   if (dtype == VBS_BF16) {
     if (vec_ok) bpd_verify_kernel<bf16_t, true><<<B, BPD_NT, 0, s>>>(logits, proposals, k, V, eos, khat, next);
     else bpd_verify_kernel<bf16_t, false><<<B, BPD_NT, 0, s>>>(logits, proposals, k, V, eos, khat, next);

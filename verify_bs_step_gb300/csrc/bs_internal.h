@@ -96,6 +96,6 @@ int launch_kv_paged_cow(const PagedArgs& a, bool bulk_ok, int num_sms, cudaStrea
 int launch_bpd_propose(const void* logits, int B, int k, int V, int dtype, bool vec_ok, int32_t* proposals,
                        cudaStream_t s);
 int launch_bpd_verify(const void* logits, const int32_t* proposals, int B, int k, int V, int dtype, bool vec_ok,
-                      int eos, int32_t* khat, int32_t* next, cudaStream_t s);
+                      int eos, int32_t* khat, int32_t* next, int* status, int num_sms, cudaStream_t s);
 
 }  // namespace vbs
