@@ -301,8 +301,8 @@ int bpd_propose(const void* logits, int B, int k, int V, int dtype, int32_t* pro
  * and an accepted proposal e < khat equals eos, khat = e + 1.
  * next[b, h] = argmax logits[b, khat-1, h, :] (the next iteration's
  * proposals).  Only the rows this needs are read.  1 <= k <= 32.
- * For B <= 65536 the call runs as a persistent work queue whose counters and
- * per-element flags are static device memory shared by every call (reset by
+ * For B <= 16384 the call runs as a persistent work queue whose counters and
+ * ready list (4 MiB) are static device memory shared by every call (reset by
  * each call's last CTA): two bpd_verify calls that overlap on the GPU
  * (different streams or host threads) race and must be serialised by the
  * caller.  A wait that gives up is reported by vbs_stateless_status().

@@ -135,8 +135,8 @@ __global__ void __launch_bounds__(BPD_NT) bpd_verify_kernel(const void* logits, 
 // of that vector equal to its maximum; one reduction over (value, lower index)
 // ---------------------------------------------------------------------------------------
 
-constexpr int BPD_RT = 512;
-constexpr int BPD_BUF = 96 * 1024;        // shared staging of one row chunk (bulk copy)
+constexpr int BPD_RT = 256;
+constexpr int BPD_BUF = 64 * 1024;        // shared staging of one row chunk (bulk copy)
 
 // The CTA's staging buffer and its mbarrier (one bulk copy in flight at a time).
 struct RowStage {
@@ -204,39 +204,43 @@ __device__ int row_argmax(const char* row, int V, RowStage& st, u64* red, int* s
 // verify + accept as a persistent work queue
 // ---------------------------------------------------------------------------------------
 //
-// Units, handed out in order by one atomic counter: unit b < B is b's verify chain (head
-// 0 at positions 0, 1, ... while the proposals agree, then head 0 at position khat-1 if
-// the chain did not read it); unit B + b*(k-1) + (h-1) is the row of head h at position
-// khat_b - 1, which waits for b's chain through a flag.  Every chain is handed out before
-// any row that waits for it, to a CTA that is already running, so no wait can block the
-// chain it waits for; waits are bounded all the same.  Only the rows the definition
-// needs are read.  The counters and flags are static device memory, reset by the last
-// CTA of each call (calls on one stream run one after the other).
+// Two kinds of work.  Chains: batch element b's verify (head 0 at positions 0, 1, ...
+// while the proposals agree, then head 0 at position khat-1 if the chain did not read
+// it), handed out in order by one counter.  Rows: head h at position khat_b - 1, h =
+// 1..k-1, which a finished chain publishes into a ready list (it reserves k-1 slots and
+// writes each as one 64-bit entry tagged with the call's epoch).  A CTA takes chains
+// while any are left, then claims ready slots in order and waits (bounded) until its
+// slot is published; every slot is reserved by a chain that is already running, so no
+// wait can block the work it waits for.  Only the rows the definition needs are read.
+// The counters and the ready list are static device memory, reset by each call's last
+// CTA (calls on one stream run one after the other).
 
-constexpr int BPD_MAX_B = 65536;
-__device__ unsigned g_bpd_flag[BPD_MAX_B];   // == epoch + 1 once b's chain is done
+constexpr int BPD_MAX_B = 16384;
+constexpr int BPD_MAX_READY = BPD_MAX_B * (KMAX - 1);
+__device__ unsigned long long g_bpd_ready[BPD_MAX_READY];   // (epoch + 1) << 32 | b << 5 | h
 __device__ unsigned g_bpd_epoch;
-__device__ int g_bpd_next_unit;
+__device__ int g_bpd_next_chain;
+__device__ int g_bpd_ready_head;
+__device__ int g_bpd_ready_tail;
 __device__ int g_bpd_exited;
 
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+__device__ __forceinline__ u64 ld_acquire_u64(const u64* p) {
+  u64 v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
-__device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+__device__ __forceinline__ void st_release_u64(u64* p, u64 v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
 }
 
 template <typename T, bool VECTOR>
-__global__ void __launch_bounds__(BPD_RT, 2) bpd_verify_queue_kernel(const void* logits, const int32_t* proposals, int B,
+__global__ void __launch_bounds__(BPD_RT, 3) bpd_verify_queue_kernel(const void* logits, const int32_t* proposals, int B,
                                                                   int k, int V, int eos, int32_t* khat_out,
                                                                   int32_t* next_out, int* status) {
   extern __shared__ __align__(128) unsigned char bpd_smem[];
   __shared__ u64 red[BPD_RT / 32 + 1];
   __shared__ __align__(8) u64 bar;
-  __shared__ int s_unit;
-  __shared__ int s_am[KMAX];
+  __shared__ int s_unit, s_b, s_h, s_q;
   const int tid = threadIdx.x;
   if (tid == 0) {
     mbar_init(&bar, 1);
@@ -244,67 +248,73 @@ __global__ void __launch_bounds__(BPD_RT, 2) bpd_verify_queue_kernel(const void*
   }
   __syncthreads();
   RowStage st{bpd_smem, &bar, 0u};
-  const unsigned epoch = *reinterpret_cast<volatile unsigned*>(&g_bpd_epoch);
+  const u64 tag = static_cast<u64>(*reinterpret_cast<volatile unsigned*>(&g_bpd_epoch) + 1u) << 32;
   const int64_t row_bytes = static_cast<int64_t>(V) * Elem<T>::BYTES;
-  const int total = B + B * (k - 1);
-  // the next unit is claimed while the current one is processed (its atomic's latency hidden)
-  int claimed = 0;
-  if (tid == 0) claimed = atomicAdd(&g_bpd_next_unit, 1);
+  const int n_rows = B * (k - 1);
+  // chains
   for (;;) {
-    if (tid == 0) s_unit = claimed;
+    if (tid == 0) s_unit = atomicAdd(&g_bpd_next_chain, 1);
     __syncthreads();
-    const int u = s_unit;
+    const int b = s_unit;
     __syncthreads();
-    if (u >= total) break;
-    if (tid == 0) claimed = atomicAdd(&g_bpd_next_unit, 1);
-    if (u < B) {
-      // b's verify chain
-      const int b = u;
-      const char* base = reinterpret_cast<const char*>(logits) + static_cast<int64_t>(b) * k * k * row_bytes;
-      const int32_t* props = proposals + static_cast<int64_t>(b) * k;
-      int checks = k - 1;                          // proposals up to an EOS need no checks past it
-      if (eos >= 0)
-        for (int e = 0; e < k; ++e)
-          if (__ldg(props + e) == eos) { checks = min(checks, e); break; }
-      int n = 1, am = -1;
-      for (int p = 0; p < checks; ++p) {
-        am = row_argmax<T, VECTOR>(base + static_cast<int64_t>(p) * k * row_bytes, V, st, red, status);
-        if (__ldg(props + p + 1) != am) break;
-        ++n;
+    if (b >= B) break;
+    const char* base = reinterpret_cast<const char*>(logits) + static_cast<int64_t>(b) * k * k * row_bytes;
+    const int32_t* props = proposals + static_cast<int64_t>(b) * k;
+    int checks = k - 1;                            // proposals up to an EOS need no checks past it
+    if (eos >= 0)
+      for (int e = 0; e < k; ++e)
+        if (__ldg(props + e) == eos) { checks = min(checks, e); break; }
+    int n = 1, am = -1;
+    for (int p = 0; p < checks; ++p) {
+      am = row_argmax<T, VECTOR>(base + static_cast<int64_t>(p) * k * row_bytes, V, st, red, status);
+      if (__ldg(props + p + 1) != am) break;
+      ++n;
+    }
+    if (n - 1 == checks)                           // khat - 1 not read by the checks: head 0 there
+      am = row_argmax<T, VECTOR>(base + static_cast<int64_t>(n - 1) * k * row_bytes, V, st, red, status);
+    if (tid == 0) {
+      khat_out[b] = n;
+      next_out[static_cast<int64_t>(b) * k] = am;
+      if (k > 1) {
+        const int slot = atomicAdd(&g_bpd_ready_tail, k - 1);
+        for (int h = 1; h < k; ++h)
+          st_release_u64(&g_bpd_ready[slot + h - 1], tag | (static_cast<u64>(b) << 5) | static_cast<u64>(h));
       }
-      if (n - 1 == checks)                         // khat - 1 not read by the checks: head 0 there
-        am = row_argmax<T, VECTOR>(base + static_cast<int64_t>(n - 1) * k * row_bytes, V, st, red, status);
-      if (tid == 0) {
-        khat_out[b] = n;
-        next_out[static_cast<int64_t>(b) * k] = am;
-        st_release_u32(&g_bpd_flag[b], epoch + 1u);
-      }
-    } else {
-      // head h at position khat_b - 1
-      const int f = u - B;
-      const int b = f / (k - 1), h = f - b * (k - 1) + 1;
-      if (tid == 0) {
-        u32 it = 0;
-        while (ld_acquire_u32(&g_bpd_flag[b]) != epoch + 1u) {
-          if (++it > (1u << 24)) { set_status(status, VBS_ETIMEOUT); break; }
-          __nanosleep(64);
-        }
-        s_am[0] = *reinterpret_cast<volatile int32_t*>(khat_out + b);
-      }
-      __syncthreads();
-      const int q = max(1, min(s_am[0], k)) - 1;
-      __syncthreads();
-      const char* row = reinterpret_cast<const char*>(logits) +
-                        ((static_cast<int64_t>(b) * k + q) * k + h) * row_bytes;
-      const int am = row_argmax<T, VECTOR>(row, V, st, red, status);
-      if (tid == 0) next_out[static_cast<int64_t>(b) * k + h] = am;
     }
   }
-  // the last CTA out resets the queue and moves the flags to the next epoch
+  // published rows: head h at position khat_b - 1
+  for (;;) {
+    if (tid == 0) {
+      const int r = atomicAdd(&g_bpd_ready_head, 1);
+      s_unit = r;
+      if (r < n_rows) {
+        u64 e = 0;
+        u32 it = 0;
+        while (((e = ld_acquire_u64(&g_bpd_ready[r])) >> 32) != (tag >> 32)) {
+          if (++it > (1u << 24)) { set_status(status, VBS_ETIMEOUT); break; }
+          __nanosleep(32);
+        }
+        const int b = static_cast<int>((e & 0xffffffffull) >> 5);
+        s_b = min(b, B - 1);
+        s_h = max(1, min(static_cast<int>(e & 31u), k - 1));
+        s_q = max(1, min(*reinterpret_cast<volatile int32_t*>(khat_out + s_b), k)) - 1;
+      }
+    }
+    __syncthreads();
+    const int r = s_unit, b = s_b, h = s_h, q = s_q;
+    __syncthreads();
+    if (r >= n_rows) break;
+    const char* row = reinterpret_cast<const char*>(logits) + ((static_cast<int64_t>(b) * k + q) * k + h) * row_bytes;
+    const int am = row_argmax<T, VECTOR>(row, V, st, red, status);
+    if (tid == 0) next_out[static_cast<int64_t>(b) * k + h] = am;
+  }
+  // the last CTA out resets the queue and moves the ready list to the next epoch
   if (tid == 0) {
     __threadfence();
     if (atomicAdd(&g_bpd_exited, 1) == static_cast<int>(gridDim.x) - 1) {
-      g_bpd_next_unit = 0;
+      g_bpd_next_chain = 0;
+      g_bpd_ready_head = 0;
+      g_bpd_ready_tail = 0;
       g_bpd_exited = 0;
       __threadfence();
       atomicAdd(&g_bpd_epoch, 1u);
@@ -363,7 +373,7 @@ int launch_bpd_verify(const void* logits, const int32_t* proposals, int B, int k
                       int eos, int32_t* khat, int32_t* next, int* status, int num_sms, cudaStream_t s) {
   if (B == 0) return VBS_OK;
   if (B <= BPD_MAX_B) {
-    const int grid = std::min(B * k, num_sms * 2);  // two CTAs (two staged rows) per SM
+    const int grid = std::min(B * k, num_sms * 3);  // three CTAs (three staged rows) per SM
     if (dtype == VBS_BF16)
       return vec_ok ? launch_queue<bf16_t, true>(grid, logits, proposals, B, k, V, eos, khat, next, status, s)
                     : launch_queue<bf16_t, false>(grid, logits, proposals, B, k, V, eos, khat, next, status, s);
