@@ -134,3 +134,22 @@ def test_blockwise_decoding_on_gpu_reproduces_greedy():
     for b in range(B):
         assert out[b][:length] == greedy[b]
     assert it < length                             # fewer iterations than greedy steps
+
+
+@pytest.mark.parametrize("B,k", [(16384, 2), (16385, 2)])
+def test_verify_on_both_sides_of_the_queue_limit(B, k):
+    """Batches up to 16384 run the work-queue kernel, larger ones the one-CTA-per-element
+    kernel; both must equal the oracle (a vectorised V = 64 keeps the rows small)."""
+    import verify_bs_step_gb300 as vbs
+    V = 64
+    base, props, heads = synth.geometric_prefix_proposals(B, k, V, seed=B, step=0)
+    logits = synth.planted_rows(heads, V, seed=B + 1, salt=2, dtype=torch.bfloat16)
+    for _ in range(2):                            # twice: the queue's state resets between calls
+        khat, nxt = vbs.bpd_verify(logits.cuda(), props.to(torch.int32).cuda())
+        torch.cuda.synchronize()
+    # the oracle on a sample of the batch (its loops are slow on 16k elements)
+    pick = np.r_[0:64, B - 64:B]
+    ekh, enx = ob.verify(_np(logits[pick]), props[pick].numpy())
+    np.testing.assert_array_equal(khat.cpu().numpy()[pick], ekh)
+    np.testing.assert_array_equal(nxt.cpu().numpy()[pick], enx)
+    assert vbs.lib().vbs_stateless_status(vbs._stream()) == 0
