@@ -138,6 +138,17 @@ VBS_EXPORT int bs_init(vbs_bs** out, int batch, int W, int V, int eos, double al
   a.per = per;
   a.P = static_cast<int>((V + per - 1) / per + 1);
   c->grid = static_cast<int>(G);
+  // cluster mode: a cluster of C CTAs per sentence (W / C whole rows each) when the
+  // sentence's 2W-best fit one warp's merge and the clusters fit one wave
+  a.cluster = 0;
+  if (W * a.K <= 32) {
+    for (int C = 4; C >= 1; C >>= 1) {
+      if (W % C == 0 && W / C <= vbs::BS_NSLOT && static_cast<int64_t>(batch) * C <= num_sms()) {
+        a.cluster = C;
+        break;
+      }
+    }
+  }
 
   Carver cv;
   for (int pass = 0; pass < 2; ++pass) {

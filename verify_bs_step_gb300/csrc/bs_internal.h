@@ -40,6 +40,7 @@ struct BsArgs {
   int* row_p0;                    // [R] the first CTA whose range holds row r
   int* row_np;                    // [R] the number of CTAs (partials) holding row r
   int* done_count;                // sentences finished (step-local counter)
+  int cluster;                    // 0: flat split + merge kernel; C: a cluster of C CTAs per sentence
   int* done;
   // finished sets
   double* fin_ns;
@@ -56,6 +57,7 @@ int launch_bs_step(const BsArgs& a, int grid, bool vector_ok, cudaStream_t s);
 int launch_bs_reset(const BsArgs& a, cudaStream_t s);
 int launch_bs_finalize(const BsArgs& a, const float* scores, const int32_t* seqs, int32_t* out_seqs,
                        int32_t* out_len, float* out_score, cudaStream_t s);
+constexpr int BS_NSLOT = 4;       // row segments one stream CTA holds (cluster mode: W / C <= this)
 int bs_threads_per_cta();
 int bs_ctas_per_sm();
 

@@ -32,6 +32,8 @@
 #include <cmath>
 #include <mutex>
 
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "bs_internal.h"
 
@@ -43,7 +45,7 @@ constexpr int BS_NT = BS_NC + 32;                 // + the producer warp
 constexpr int BS_U = 4;                           // 16-byte vectors per consumer per chunk
 constexpr int STAGE_BYTES = BS_NC * BS_U * 16;    // 32 KiB
 constexpr int NSTAGE = 6;
-constexpr int NSLOT = 4;                          // row segments held before they are published
+constexpr int NSLOT = BS_NSLOT;                   // row segments held before they are published
 constexpr int QSEG = 512;                         // candidate queue of one segment
 constexpr int QSTEP = 8;                          // threshold refresh once QSTEP more keys are queued
 constexpr int FIN_CAP = 256;                      // keys collected at a segment's final bar
@@ -52,6 +54,9 @@ constexpr int SEQ_TILE_INTS = 2048;               // sequence gather tile (all W
 constexpr int BAR_CONSUMERS = 1;                  // named barrier of the consumer warps
 constexpr int MG_NT = 256;                        // merge kernel threads
 constexpr int MG_NW = MG_NT / 32;
+// fp32 ln 2 split in two: LN2_HI = fl(ln 2), LN2_LO = ln 2 - LN2_HI.
+constexpr float LN2_HI = 0.693147182464599609375f;
+constexpr float LN2_LO = -1.904654299957768e-09f;
 
 // Merge (M, l) pairs in the log2 domain: sum = l * 2^M.
 __device__ __forceinline__ void lse_merge(float& M, float& l, float M2, float l2) {
@@ -128,6 +133,13 @@ struct BsShared {                              // the stream kernel
   int mode[NSLOT];                             // 0: tiles resolved, 1: needs a rescan, 2: q holds keys
   int seg_r[NSLOT], seg_v0[NSLOT], seg_v1[NSLOT], seg_skip[NSLOT];
   int stage_skip[NSTAGE];                      // the producer's skip decision for each ring stage
+  // cluster mode: this CTA's whole rows (K best keys, sorted; max and scaled sum)
+  u64 rk[NSLOT][KMAX];
+  float rM[NSLOT], rl[NSLOT];
+  // cluster mode: the sentence merge's candidates (one per lane)
+  u64 cm_key[32];
+  float cm_c[32];
+  int cm_w[32], cm_sel[32];
 };
 
 struct MergeShared {                           // the merge kernel
@@ -373,8 +385,9 @@ __device__ void finish_segment(const BsArgs& a, BsShared& sh, int s, int lane) {
       lse_merge(Mw, lw, M2, l2);
     }
     const int r = sh.seg_r[s];
-    const int64_t pslot = static_cast<int64_t>(r) * a.P + (static_cast<int>(blockIdx.x) - a.row_p0[r]);
-    u64* out = a.part_key + pslot * K;
+    const int64_t pslot =
+        a.cluster ? 0 : static_cast<int64_t>(r) * a.P + (static_cast<int>(blockIdx.x) - a.row_p0[r]);
+    u64* out = a.cluster ? sh.rk[s] : a.part_key + pslot * K;   // cluster mode: whole rows stay in shared memory
     if (mode == 0) {
       const int cnt = sh.fcnt[s];
       for (int j = lane; j < cnt; j += 32) {
@@ -388,7 +401,15 @@ __device__ void finish_segment(const BsArgs& a, BsShared& sh, int s, int lane) {
       warp_select_topk(sh.q[s], min(sh.qcnt[s], QSEG), K, sh.fin[s], lane);
       if (lane < K) out[lane] = sh.fin[s][lane];
     }
-    if (lane == 0) { a.part_M[pslot] = Mw; a.part_l[pslot] = lw; }
+    if (lane == 0) {
+      if (a.cluster) {
+        sh.rM[s] = Mw;
+        sh.rl[s] = lw;
+      } else {
+        a.part_M[pslot] = Mw;
+        a.part_l[pslot] = lw;
+      }
+    }
   }
   __syncwarp();
   const int n = mode == 0 ? min(sh.qcnt[s], QSEG) : QSEG;
@@ -582,6 +603,258 @@ __global__ void __launch_bounds__(BS_NT, 1) bs_stream_kernel(const BsArgs a) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+
+// ---------------------------------------------------------------------------------------
+// cluster mode: a cluster of C CTAs per sentence, each CTA streaming W/C whole rows
+// ---------------------------------------------------------------------------------------
+//
+// When W * 2W <= 32 and B * C CTAs fit one wave, sentence b is owned by the cluster of C
+// CTAs b*C .. b*C+C-1, CTA c streaming rows b*W + c*(W/C) .. + W/C - 1 whole.  Each CTA
+// leaves its rows' K best keys and (max, scaled sum) in its own shared memory; after a
+// cluster barrier one warp of the cluster's first CTA reads them through distributed
+// shared memory and merges the sentence: no partials in global memory, no second kernel.
+
+constexpr int CM_TILE = 8192;                      // sequence staging (ints), in the free ring
+
+// One warp: sentence b's merge from the cluster's row results (W * K <= 32; lane = w*K + i).
+__device__ void cluster_merge_sentence(const BsArgs& a, BsShared& sh, int b, int lane) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cl = cg::this_cluster();
+  const int W = a.W, K = a.K, RPC = W / a.cluster;
+  const int r0 = b * W, t = a.t, ld = a.seq_ld;
+  int* tile = reinterpret_cast<int*>(&sh.ring[0][0]);
+  // ---- one round of loads: the rows' results (distributed shared memory), the sentence state
+  const int wl = min(lane / K, W - 1), il = lane - wl * K;
+  u64 kl = 0ull;
+  if (lane < W * K) kl = cl.map_shared_rank(&sh, wl / RPC)->rk[wl % RPC][il];
+  float Mr = -INFINITY, lr = 0.f, s_row = 0.f, fns = 0.f;
+  int flen = 0, fser = 0;
+  if (lane < W) {
+    const BsShared* src = cl.map_shared_rank(&sh, lane / RPC);
+    Mr = src->rM[lane % RPC];
+    lr = src->rl[lane % RPC];
+    s_row = __ldcg(a.scores + r0 + lane);
+    fns = static_cast<float>(__ldcg(a.fin_ns + r0 + lane));
+    flen = __ldcg(a.fin_len + r0 + lane);
+    fser = __ldcg(a.fin_serial + r0 + lane);
+  }
+  int fcount = 0, fnext = 0;
+  float fworst = 0.f;
+  if (lane == 0) {
+    fcount = __ldcg(a.fin_count + b);
+    fnext = __ldcg(a.fin_next + b);
+    fworst = static_cast<float>(__ldcg(a.fin_worst + b));
+  }
+  const bool was_done = __ldcg(a.done + b) != 0;
+  fcount = __shfl_sync(FULL, fcount, 0);
+  fnext = __shfl_sync(FULL, fnext, 0);
+  fworst = __shfl_sync(FULL, fworst, 0);
+  unsigned old_cnt = 0;
+  int done_now = 1;
+  int nb_row = r0, nb_tok = a.pad, f_src = -1;     // lane w < W: new beam w, finished slot w's source
+  float nb_score = 0.f;
+  if (!was_done) {
+    // ---- row LSEs as fp32 pairs hi + lo (lanes < W), then the candidates' scores
+    float hi = 0.f, lo = 0.f;
+    if (lane < W && s_row != -INFINITY) {
+      const float L2 = log2f(lr);
+      const float t_hi = Mr + L2;
+      const float bb = t_hi - Mr;
+      const float t_lo = (Mr - (t_hi - bb)) + (L2 - bb);
+      const float p2 = t_hi * LN2_HI;
+      const float e = fmaf(t_hi, LN2_HI, -p2) + fmaf(t_hi, LN2_LO, t_lo * LN2_HI);
+      hi = p2 + e;
+      lo = e - (hi - p2);
+      if (!(hi > -INFINITY && hi < INFINITY)) set_status(a.status, VBS_EINPUT);  // no finite logit, NaN, +inf
+    }
+    const float sw = __shfl_sync(FULL, s_row, wl);
+    const float hw = __shfl_sync(FULL, hi, wl), lw = __shfl_sync(FULL, lo, wl);
+    float cl_ = -INFINITY;
+    if (lane < W * K) {
+      if (sw == -INFINITY) {                       // a row at -inf: -inf candidates by token id
+        kl = il < min(K, a.V) ? make_key(-INFINITY, static_cast<u32>(il)) : 0ull;
+      } else {
+        const float x = key_x(kl);
+        if (kl != 0ull && x != -INFINITY) cl_ = sw + ((x - hw) - lw);
+      }
+    } else {
+      kl = 0ull;
+    }
+    // ---- the sentence's ranking: (score desc, list position asc) = (score desc, flat index asc)
+    const int nvalid = __popc(__ballot_sync(FULL, kl != 0ull));
+    {
+      const int rank = warp_rank_u32(kl != 0ull ? ord_f32(cl_) : 0u, lane);
+      if (kl != 0ull && rank < 2 * W) sh.cm_sel[rank] = lane;
+    }
+    sh.cm_key[lane] = kl;
+    sh.cm_c[lane] = cl_;
+    sh.cm_w[lane] = wl;
+    __syncwarp();
+    // ---- the walk, one lane per rank (2W <= 32): the k-th candidate that is not an EOS hit
+    // becomes new beam k, for k < W; an EOS hit at rank < W that the walk reaches joins the
+    // finished set, in rank order
+    const bool have = lane < 2 * W && lane < nvalid;
+    const int jw = have ? sh.cm_sel[lane] : 0;
+    const u64 kw = have ? sh.cm_key[jw] : 0ull;
+    const float cw = have ? sh.cm_c[jw] : -INFINITY;
+    const int ww = have ? sh.cm_w[jw] : 0;
+    const u32 v = key_v(kw);
+    const bool eos = have && a.eos >= 0 && v == static_cast<u32>(a.eos);
+    const u32 live = __ballot_sync(FULL, have && !eos);
+    const int before = __popc(live & ((1u << lane) - 1u));
+    const unsigned sl = __fns(live, 0, lane + 1);  // the (lane+1)-th live lane, if any
+    const int src_lane = sl < 32u ? static_cast<int>(sl) : 0;
+    const float c_in = __shfl_sync(FULL, cw, src_lane);
+    const u32 v_in = __shfl_sync(FULL, v, src_lane);
+    const int w_in = __shfl_sync(FULL, ww, src_lane);
+    const int new_cnt = min(__popc(live), W);
+    if (lane < new_cnt) {
+      nb_score = c_in;
+      nb_tok = static_cast<int>(v_in);
+      nb_row = r0 + w_in;
+    } else if (lane < W) {
+      nb_score = -INFINITY;
+    }
+    const u32 hits = __ballot_sync(FULL, eos && lane < W && before < W);
+    const float best = __shfl_sync(FULL, cw, 0);
+    // BeamHypotheses.add for each EOS hit, in rank order (slot q lives in lane q)
+    float f_ns = fns;
+    int f_len = flen, f_ser = fser;
+    for (u32 m = hits; m; m &= m - 1) {
+      const int rank = __ffs(m) - 1;
+      const float ns = __shfl_sync(FULL, cw, rank) / a.lp_tf;
+      const int src = r0 + __shfl_sync(FULL, ww, rank);
+      int slot = -1;
+      if (fcount < W) {
+        slot = fcount;
+      } else if (ns > fworst) {                    // evict the worst; ties: the earliest inserted
+        float bn = lane < W ? f_ns : INFINITY;
+        int bs2 = lane < W ? f_ser : 0x7fffffff, bl = lane;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          const float on = __shfl_xor_sync(FULL, bn, off);
+          const int os = __shfl_xor_sync(FULL, bs2, off);
+          const int ol = __shfl_xor_sync(FULL, bl, off);
+          if (on < bn || (on == bn && (os < bs2 || (os == bs2 && ol < bl)))) { bn = on; bs2 = os; bl = ol; }
+        }
+        slot = bl;
+      }
+      if (slot >= 0) {
+        if (lane == slot) {
+          f_ns = ns;
+          f_len = t;
+          f_ser = fnext;
+          f_src = src;
+        }
+        fnext += 1;
+        if (fcount < W) {
+          fcount += 1;
+          fworst = fminf(ns, fworst);
+        }
+        if (fcount >= W) {
+          float wmin = lane < W ? f_ns : INFINITY;
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) wmin = fminf(wmin, __shfl_xor_sync(FULL, wmin, off));
+          fworst = wmin;
+        }
+      }
+    }
+    if (lane == 0 && new_cnt < W) set_status(a.status, VBS_EINPUT);
+    bool done = false;
+    if (fcount >= W) done = a.early_stopping == VBS_ES_TRUE || fworst >= best / a.lp_boundf;
+    done_now = done ? 1 : 0;
+    // the step's finished-sentence count, issued before the writes
+    if (lane == 0) old_cnt = atomicAdd(reinterpret_cast<unsigned*>(a.done_count), (1u << 16) | done_now);
+    if (lane < W) {
+      a.beam_idx[r0 + lane] = nb_row;
+      a.tokens[r0 + lane] = nb_tok;
+      a.scores[r0 + lane] = nb_score;
+      a.fin_ns[r0 + lane] = static_cast<double>(f_ns);
+      a.fin_len[r0 + lane] = f_len;
+      a.fin_serial[r0 + lane] = f_ser;
+    }
+    if (lane == 0) {
+      a.fin_count[b] = fcount;
+      a.fin_next[b] = fnext;
+      a.fin_worst[b] = static_cast<double>(fworst);
+      a.done[b] = done_now;
+    }
+    // sequences: the parents' columns [0, t) gathered in place, staged one column tile at a
+    // time, then the new token at column t
+    const int TWc = CM_TILE / W;
+    for (int c0 = 0; c0 < t; c0 += TWc) {
+      const int nc = min(TWc, t - c0);
+      for (int i = lane; i < W * nc; i += 32) {
+        const int w = i / nc, c = i - w * nc;
+        tile[w * TWc + c] = __ldcg(a.seqs + static_cast<int64_t>(r0 + w) * ld + c0 + c);
+      }
+      __syncwarp();
+      for (int w = 0; w < W; ++w) {
+        const int pr = __shfl_sync(FULL, nb_row, w) - r0;
+        const int fs = __shfl_sync(FULL, f_src, w);
+        for (int c = lane; c < nc; c += 32) {
+          a.seqs[static_cast<int64_t>(r0 + w) * ld + c0 + c] = tile[pr * TWc + c];
+          if (fs >= 0) a.fin_tok[static_cast<int64_t>(r0 + w) * ld + c0 + c] = tile[(fs - r0) * TWc + c];
+        }
+      }
+      __syncwarp();
+    }
+    if (lane < W) a.seqs[static_cast<int64_t>(r0 + lane) * ld + t] = nb_tok;
+  } else {
+    if (lane == 0) old_cnt = atomicAdd(reinterpret_cast<unsigned*>(a.done_count), (1u << 16) | 1u);
+    if (lane < W) {
+      a.beam_idx[r0 + lane] = -1;
+      a.tokens[r0 + lane] = a.pad;
+      a.scores[r0 + lane] = 0.f;
+      a.seqs[static_cast<int64_t>(r0 + lane) * ld + t] = a.pad;
+    }
+  }
+  // the last sentence of the step reports whether all are finished
+  if (lane == 0 && (old_cnt >> 16) == static_cast<unsigned>(a.B - 1)) {
+    const int all = static_cast<int>((old_cnt & 0xffffu) + done_now) == a.B;
+    *a.all_done_dev = all;
+    if (a.all_done_out) *a.all_done_out = all;
+    *a.done_count = 0;
+  }
+}
+
+template <typename T, bool TMA>
+__global__ void __launch_bounds__(BS_NT, 1) bs_cluster_kernel(const BsArgs a) {
+  extern __shared__ __align__(128) unsigned char bs_smem[];
+  BsShared& sh = *reinterpret_cast<BsShared*>(bs_smem);
+  const int C = a.cluster;
+  const int b = static_cast<int>(blockIdx.x) / C, c = static_cast<int>(blockIdx.x) - b * C;
+  const int RPC = a.W / C;
+  const int64_t e0 = (static_cast<int64_t>(b) * a.W + c * RPC) * a.V;
+  const int64_t e1 = e0 + static_cast<int64_t>(RPC) * a.V;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(&sh.full[s], 1);
+      mbar_init(&sh.empty[s], BS_NCW);
+    }
+    fence_mbar_init();
+  }
+  if (threadIdx.x < NSLOT) {
+    sh.thr[threadIdx.x] = 0u;
+    sh.qcnt[threadIdx.x] = 0;
+    sh.qref[threadIdx.x] = 0;
+    sh.mode[threadIdx.x] = 0;
+  }
+  for (int i = threadIdx.x; i < NSLOT * QSEG; i += BS_NT) (&sh.q[0][0])[i] = 0ull;
+  __syncthreads();
+  if ((threadIdx.x >> 5) == BS_NCW) {
+    if constexpr (TMA) {
+      if ((threadIdx.x & 31) == 0) produce<T>(a, sh, e0, e1);
+    }
+  } else {
+    consume<T, TMA>(a, sh, e0, e1);
+  }
+  __syncwarp();
+  cooperative_groups::this_cluster().sync();       // every CTA's row results are in its shared memory
+  if (c == 0 && threadIdx.x < 32) cluster_merge_sentence(a, sh, b, threadIdx.x);
+  cooperative_groups::this_cluster().sync();       // keep them readable until the merge is done
+}
+
 // ---------------------------------------------------------------------------------------
 // the merge kernel: one CTA per sentence
 // ---------------------------------------------------------------------------------------
@@ -612,9 +885,7 @@ __device__ void merge_prefetch_rows(const BsArgs& a, MergeShared& sm, int b) {
   }
 }
 
-// fp32 ln 2 split in two: LN2_HI = fl(ln 2), LN2_LO = ln 2 - LN2_HI.
-constexpr float LN2_HI = 0.693147182464599609375f;
-constexpr float LN2_LO = -1.904654299957768e-09f;
+
 
 // Warp-wide, from the prefetched partials: row w's LSE (split hi + lo in fp32) and its
 // sorted top-K list with scores.
@@ -1008,7 +1279,36 @@ static int launch_merge(const BsArgs& a, cudaStream_t s) {
   return cudaLaunchKernelEx(&cfg, bs_merge_kernel, a) == cudaSuccess ? VBS_OK : VBS_ECUDA;
 }
 
+template <typename T, bool TMA>
+static int launch_cluster(const BsArgs& a, cudaStream_t s) {
+  static bool attr_set = false;
+  const int smem = static_cast<int>(sizeof(BsShared));
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(bs_cluster_kernel<T, TMA>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+      return VBS_ECUDA;
+    attr_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.B * a.cluster);
+  cfg.blockDim = dim3(BS_NT);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = a.cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, bs_cluster_kernel<T, TMA>, a) == cudaSuccess ? VBS_OK : VBS_ECUDA;
+}
+
 int launch_bs_step(const BsArgs& a, int grid, bool vector_ok, cudaStream_t s) {
+  if (a.cluster) {
+    if (a.dtype == VBS_BF16) return vector_ok ? launch_cluster<bf16_t, true>(a, s) : launch_cluster<bf16_t, false>(a, s);
+    return vector_ok ? launch_cluster<float, true>(a, s) : launch_cluster<float, false>(a, s);
+  }
   int st;
   if (a.dtype == VBS_BF16)
     st = vector_ok ? launch_stream<bf16_t, true>(a, grid, s) : launch_stream<bf16_t, false>(a, grid, s);
