@@ -48,7 +48,8 @@ constexpr int NSTAGE = 6;
 constexpr int NSLOT = BS_NSLOT;                   // row segments held before they are published
 constexpr int QSEG = 512;                         // candidate queue of one segment
 constexpr int QSTEP = 8;                          // threshold refresh once QSTEP more keys are queued
-constexpr int FIN_CAP = 256;                      // keys collected at a segment's final bar
+constexpr int FIN_CAP = 64;                       // keys collected at a segment's final bar
+constexpr int PF_TILE = 1024;                     // cluster mode: sequence columns prefetched (ints)
 constexpr int CT_CAP = 64;                        // tiles re-read at a segment's final bar
 constexpr int SEQ_TILE_INTS = 2048;               // sequence gather tile (all W rows)
 constexpr int BAR_CONSUMERS = 1;                  // named barrier of the consumer warps
@@ -140,6 +141,11 @@ struct BsShared {                              // the stream kernel
   u64 cm_key[32];
   float cm_c[32];
   int cm_w[32], cm_sel[32];
+  // cluster mode: the merge's inputs this kernel does not write, prefetched at its start
+  int pf_tile[PF_TILE];
+  double pf_fns[WMAX], pf_fworst;
+  float pf_s[WMAX];
+  int pf_flen[WMAX], pf_fser[WMAX], pf_fcount, pf_fnext, pf_done;
 };
 
 struct MergeShared {                           // the merge kernel
@@ -616,6 +622,39 @@ __global__ void __launch_bounds__(BS_NT, 1) bs_stream_kernel(const BsArgs a) {
 
 constexpr int CM_TILE = 8192;                      // sequence staging (ints), in the free ring
 
+__device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" :: "r"(smem_u32(smem)), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async8(void* smem, const void* gmem) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" :: "r"(smem_u32(smem)), "l"(gmem) : "memory");
+}
+
+// One warp of the cluster's first CTA, at the kernel's start: the sentence state and the
+// first sequence columns (written by earlier kernels only) are copied into shared memory
+// asynchronously, to be ready when the merge needs them.
+__device__ void cluster_prefetch(const BsArgs& a, BsShared& sh, int b, int lane) {
+  const int W = a.W, r0 = b * W, ld = a.seq_ld;
+  const int TWp = PF_TILE / W;
+  const int nc = min(a.t, TWp);
+  for (int i = lane; i < W * nc; i += 32) {
+    const int w = i / nc, c = i - w * nc;
+    cp_async4(&sh.pf_tile[w * TWp + c], a.seqs + static_cast<int64_t>(r0 + w) * ld + c);
+  }
+  if (lane < W) {
+    cp_async4(&sh.pf_s[lane], a.scores + r0 + lane);
+    cp_async8(&sh.pf_fns[lane], a.fin_ns + r0 + lane);
+    cp_async4(&sh.pf_flen[lane], a.fin_len + r0 + lane);
+    cp_async4(&sh.pf_fser[lane], a.fin_serial + r0 + lane);
+  }
+  if (lane == 0) {
+    cp_async4(&sh.pf_fcount, a.fin_count + b);
+    cp_async4(&sh.pf_fnext, a.fin_next + b);
+    cp_async8(&sh.pf_fworst, a.fin_worst + b);
+    cp_async4(&sh.pf_done, a.done + b);
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
 // One warp: sentence b's merge from the cluster's row results (W * K <= 32; lane = w*K + i).
 __device__ void cluster_merge_sentence(const BsArgs& a, BsShared& sh, int b, int lane) {
   namespace cg = cooperative_groups;
@@ -627,28 +666,22 @@ __device__ void cluster_merge_sentence(const BsArgs& a, BsShared& sh, int b, int
   const int wl = min(lane / K, W - 1), il = lane - wl * K;
   u64 kl = 0ull;
   if (lane < W * K) kl = cl.map_shared_rank(&sh, wl / RPC)->rk[wl % RPC][il];
+  asm volatile("cp.async.wait_all;" ::: "memory");   // this warp's prefetch of the sentence state
+  __syncwarp();
   float Mr = -INFINITY, lr = 0.f, s_row = 0.f, fns = 0.f;
   int flen = 0, fser = 0;
   if (lane < W) {
     const BsShared* src = cl.map_shared_rank(&sh, lane / RPC);
     Mr = src->rM[lane % RPC];
     lr = src->rl[lane % RPC];
-    s_row = __ldcg(a.scores + r0 + lane);
-    fns = static_cast<float>(__ldcg(a.fin_ns + r0 + lane));
-    flen = __ldcg(a.fin_len + r0 + lane);
-    fser = __ldcg(a.fin_serial + r0 + lane);
+    s_row = sh.pf_s[lane];
+    fns = static_cast<float>(sh.pf_fns[lane]);
+    flen = sh.pf_flen[lane];
+    fser = sh.pf_fser[lane];
   }
-  int fcount = 0, fnext = 0;
-  float fworst = 0.f;
-  if (lane == 0) {
-    fcount = __ldcg(a.fin_count + b);
-    fnext = __ldcg(a.fin_next + b);
-    fworst = static_cast<float>(__ldcg(a.fin_worst + b));
-  }
-  const bool was_done = __ldcg(a.done + b) != 0;
-  fcount = __shfl_sync(FULL, fcount, 0);
-  fnext = __shfl_sync(FULL, fnext, 0);
-  fworst = __shfl_sync(FULL, fworst, 0);
+  int fcount = sh.pf_fcount, fnext = sh.pf_fnext;
+  float fworst = static_cast<float>(sh.pf_fworst);
+  const bool was_done = sh.pf_done != 0;
   unsigned old_cnt = 0;
   int done_now = 1;
   int nb_row = r0, nb_tok = a.pad, f_src = -1;     // lane w < W: new beam w, finished slot w's source
@@ -781,8 +814,17 @@ __device__ void cluster_merge_sentence(const BsArgs& a, BsShared& sh, int b, int
     }
     // sequences: the parents' columns [0, t) gathered in place, staged one column tile at a
     // time, then the new token at column t
+    const int TWp = PF_TILE / W, ncp = min(t, TWp);
+    for (int w = 0; w < W; ++w) {                  // the prefetched columns
+      const int pr = __shfl_sync(FULL, nb_row, w) - r0;
+      const int fs = __shfl_sync(FULL, f_src, w);
+      for (int c = lane; c < ncp; c += 32) {
+        a.seqs[static_cast<int64_t>(r0 + w) * ld + c] = sh.pf_tile[pr * TWp + c];
+        if (fs >= 0) a.fin_tok[static_cast<int64_t>(r0 + w) * ld + c] = sh.pf_tile[(fs - r0) * TWp + c];
+      }
+    }
     const int TWc = CM_TILE / W;
-    for (int c0 = 0; c0 < t; c0 += TWc) {
+    for (int c0 = ncp; c0 < t; c0 += TWc) {        // the rest, staged through the free ring
       const int nc = min(TWc, t - c0);
       for (int i = lane; i < W * nc; i += 32) {
         const int w = i / nc, c = i - w * nc;
@@ -847,6 +889,7 @@ __global__ void __launch_bounds__(BS_NT, 1) bs_cluster_kernel(const BsArgs a) {
       if ((threadIdx.x & 31) == 0) produce<T>(a, sh, e0, e1);
     }
   } else {
+    if (c == 0 && threadIdx.x < 32) cluster_prefetch(a, sh, b, threadIdx.x);
     consume<T, TMA>(a, sh, e0, e1);
   }
   __syncwarp();
