@@ -28,7 +28,7 @@ import torch
 
 _MASK64 = (1 << 64) - 1
 
-SIGMA = {"tiny": 2.0, "tbase": 3.0, "llama": 2.5, "sweep": 2.0, "bpd": 2.0}
+SIGMA = {"tiny": 2.0, "tbase": 3.0, "llama": 2.5, "sweep": 2.0, "bpd": 2.0, "ramp": 1.0}
 
 
 def mix_seed(*coords: int) -> int:
@@ -80,6 +80,10 @@ def beam_logits(kind: str, W: int, V: int, *, seed: int, step: int, sentence: in
             lift = 0.5 + 1.5 * torch.rand(W, generator=g, device=device)
             rowmax = x.max(dim=1).values
             x[:, eos] = torch.where(hit, rowmax + lift, x[:, eos])
+    elif kind == "ramp":
+        # logits rising along the vocabulary (+12 over the row): each stretch of the row
+        # beats everything before it, the worst order for a running top-k threshold
+        x += torch.arange(V, device=device, dtype=torch.float32) * (12.0 / V)
     elif kind not in ("tiny",):
         raise ValueError(f"unknown logits kind {kind!r}")
     return x.to(dtype)

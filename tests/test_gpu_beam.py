@@ -168,6 +168,16 @@ def test_shapes(B, W, V, dtype, ld_pad):
     _run(case)
 
 
+@pytest.mark.parametrize("B,W,V,dtype", [
+    (3, 4, 32000, torch.float32),         # vector path: the queue overflows, rows are rescanned
+    (2, 3, 20011, torch.float32),         # element path, ragged tail
+    (1, 2, 128256, torch.bfloat16),
+])
+def test_ascending_rows(B, W, V, dtype):
+    case = hz.BeamCase("ramp", B, W, V, 4, dtype, eos=5, seed=B * 31 + V % 1009)
+    _run(case)
+
+
 def test_eos_heavy_until_all_done_and_reset():
     import verify_bs_step_gb300 as vbs
     # V = 8 with EOS: sentences finish within a few steps; then the whole batch is padded

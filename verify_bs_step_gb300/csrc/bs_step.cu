@@ -344,8 +344,9 @@ __device__ void resolve_tiles(const BsArgs& a, BsShared& sh, int s, int lane) {
 // segment at or above a bar, re-reading the segment from global memory, until one pass
 // fits in the queue; each pass that overflows raises the bar to the K-th best key it
 // queued (keys are distinct and QSEG > K, so the bar rises and the passes end).  Only
-// ties at the bar and adversarial orders (e.g. ascending logits) get here.
-template <typename T>
+// ties at the bar and adversarial orders (e.g. ascending logits) get here.  The aligned
+// path reads 16-byte vectors: the segment may have left L2 by now.
+template <typename T, int VEC>
 __device__ void rescan_segment(const BsArgs& a, BsShared& sh, int s) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K = a.K;
@@ -358,11 +359,17 @@ __device__ void rescan_segment(const BsArgs& a, BsShared& sh, int s) {
     for (int i = tid; i < QSEG; i += BS_NC) sh.q[s][i] = 0ull;
     if (tid == 0) sh.qcnt[s] = 0;
     named_sync(BAR_CONSUMERS, BS_NC);
-    for (int v = sv0 + tid; v < sv1; v += BS_NC) {
-      const u64 k = make_key(Elem<T>::load(row, v), static_cast<u32>(v));
-      if (k >= bar) {
-        const int pos = atomicAdd(&sh.qcnt[s], 1);
-        if (pos < QSEG) sh.q[s][pos] = k;
+    for (int v = sv0 + tid * VEC; v < sv1; v += BS_NC * VEC) {
+      float x[VEC];
+      if constexpr (VEC == 1) x[0] = Elem<T>::load(row, v);
+      else Vec16<T>::unpack(ld_stream16(row + static_cast<int64_t>(v) * Elem<T>::BYTES), x);
+#pragma unroll
+      for (int e2 = 0; e2 < VEC; ++e2) {
+        const u64 k = make_key(x[e2], static_cast<u32>(v + e2));
+        if (k >= bar) {
+          const int pos = atomicAdd(&sh.qcnt[s], 1);
+          if (pos < QSEG) sh.q[s][pos] = k;
+        }
       }
     }
     named_sync(BAR_CONSUMERS, BS_NC);
@@ -430,7 +437,7 @@ __device__ void publish_slots(const BsArgs& a, BsShared& sh, int ns) {
   if (warp < ns && !sh.seg_skip[warp]) resolve_tiles<T, VEC>(a, sh, warp, lane);
   named_sync(BAR_CONSUMERS, BS_NC);
   for (int s = 0; s < ns; ++s)
-    if (!sh.seg_skip[s] && sh.mode[s] == 1) rescan_segment<T>(a, sh, s);
+    if (!sh.seg_skip[s] && sh.mode[s] == 1) rescan_segment<T, VEC>(a, sh, s);
   if (warp < ns) finish_segment(a, sh, warp, lane);
 }
 
@@ -538,12 +545,13 @@ __device__ void consume(const BsArgs& a, BsShared& sh, int64_t e0, int64_t e1) {
       u32 thr_o = *reinterpret_cast<volatile u32*>(&sh.thr[slot]);
       const u32 tmo = tm > -INFINITY ? ord_f32(tm) : 0u;
       if (!seeded) {
+        // every consumer warp is at the segment's first chunk: the threshold starts at
+        // the best of the warps' seeds, so only a few tiles of this chunk are queued
         seeded = true;
         const u32 seed = warp_kth_u32(tmo, K, lane);
-        if (seed > thr_o) {
-          if (lane == 0) atomicMax(&sh.thr[slot], seed);
-          thr_o = seed;
-        }
+        if (lane == 0 && seed > thr_o) atomicMax(&sh.thr[slot], seed);
+        named_sync(BAR_CONSUMERS, BS_NC);
+        thr_o = *reinterpret_cast<volatile u32*>(&sh.thr[slot]);
       }
       if (tmo != 0u && tmo >= thr_o) {
         const int pos = atomicAdd(&sh.qcnt[slot], 1);
