@@ -121,8 +121,9 @@ __device__ void warp_merge_sorted(const u64* lists, int nl, int K, u64* out, int
 struct BsShared {                              // the stream kernel
   unsigned char ring[NSTAGE][STAGE_BYTES];     // the streamed chunks
   u64 q[NSLOT][QSEG];                          // hot tiles (max, position) per row segment; keys after a rescan
+  u32 qd[NSLOT][QSEG];                         // per hot tile: a bound on its second-largest value | max's place
   u64 fin[NSLOT][FIN_CAP];                     // a segment's final candidate keys
-  u32 ctile[NSLOT][CT_CAP];                    // a segment's final candidate tiles
+  u32 ctile[NSLOT][CT_CAP];                    // a segment's final candidate tiles (queue indices)
   float M[NSLOT][BS_NCW], l[NSLOT][BS_NCW];    // per-warp (max, scaled sum) of each segment
   u64 full[NSTAGE], empty[NSTAGE];
   u64 rbar[NSLOT];                             // the key bar of a rescan
@@ -147,6 +148,8 @@ struct BsShared {                              // the stream kernel
   float pf_s[WMAX];
   int pf_flen[WMAX], pf_fser[WMAX], pf_fcount, pf_fnext, pf_done;
 };
+
+static_assert(sizeof(BsShared) <= 232448, "the stream kernel's shared memory fits one SM");
 
 struct MergeShared {                           // the merge kernel
   u64 rowscratch[WMAX * PART_KEYS];            // the rows' partial lists
@@ -304,7 +307,7 @@ __device__ void resolve_tiles(const BsArgs& a, BsShared& sh, int s, int lane) {
     const bool cand = e != 0 && static_cast<u32>(e >> 32) >= bar;
     const u32 b = __ballot_sync(FULL, cand);
     const int pos = nc + __popc(b & ((1u << lane) - 1u));
-    if (cand && pos < CT_CAP) sh.ctile[s][pos] = static_cast<u32>(e);
+    if (cand && pos < CT_CAP) sh.ctile[s][pos] = static_cast<u32>(j);
     nc += __popc(b);
   }
   __syncwarp();
@@ -316,7 +319,17 @@ __device__ void resolve_tiles(const BsArgs& a, BsShared& sh, int s, int lane) {
   const int sv1 = sh.seg_v1[s];
   const char* row = reinterpret_cast<const char*>(a.logits) + static_cast<int64_t>(sh.seg_r[s]) * a.ld * Elem<T>::BYTES;
   for (int t = lane; t < nc; t += 32) {
-    const u32 vb = sh.ctile[s][t];
+    const int jq = static_cast<int>(sh.ctile[s][t]);
+    const u64 eq = sh.q[s][jq];
+    const u32 vb = static_cast<u32>(eq);
+    const u32 desc = sh.qd[s][jq];
+    if ((desc & ~31u) <= bar) {
+      // every other element of the tile lies below the bar: the maximum is the only key
+      const u32 pu = (desc & 31u) / VEC, pe = (desc & 31u) % VEC;
+      const int p = atomicAdd(&sh.fcnt[s], 1);
+      if (p < FIN_CAP) sh.fin[s][p] = make_key(unord_f32(static_cast<u32>(eq >> 32)), vb + pu * (BS_NC * VEC) + pe);
+      continue;
+    }
 #pragma unroll
     for (int u = 0; u < BS_U; ++u) {
       const u32 v0 = vb + static_cast<u32>(u * BS_NC * VEC);
@@ -511,6 +524,60 @@ __device__ void consume(const BsArgs& a, BsShared& sh, int64_t e0, int64_t e1) {
 #pragma unroll
         for (int u = 1; u < BS_U; ++u) tm = fmaxf(tm, xs[u]);
       }
+      // the threshold: each warp seeds it at the segment's first chunk with the K-th best
+      // of its lane maxima; one warp per chunk raises it from the queue once QSTEP more
+      // tiles have been queued
+      u32 thr_o = *reinterpret_cast<volatile u32*>(&sh.thr[slot]);
+      const u32 tmo = tm > -INFINITY ? ord_f32(tm) : 0u;
+      if (!seeded) {
+        // every consumer warp is at the segment's first chunk: the threshold starts at
+        // the best of the warps' seeds, so only a few tiles of this chunk are queued
+        seeded = true;
+        const u32 seed = warp_kth_u32(tmo, K, lane);
+        if (lane == 0 && seed > thr_o) atomicMax(&sh.thr[slot], seed);
+        named_sync(BAR_CONSUMERS, BS_NC);
+        thr_o = *reinterpret_cast<volatile u32*>(&sh.thr[slot]);
+      }
+      if (tmo != 0u && tmo >= thr_o) {
+        // also record where the maximum sits (vector um, element em) and a bound on the
+        // tile's second-largest value, so that the final resolve seldom reads the tile
+        // again; signed zeros compare equal as floats, so a zero maximum or runner-up
+        // leaves the descriptor unknown
+        int um = -1, em = -1;
+        float sec = -INFINITY;
+        uint4 qm = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int u = 0; u < BS_U; ++u) {
+          float vmu;
+          if constexpr (TMA) vmu = VecMax<T>::finish(VecMax<T>::fold(q[u], VecMax<T>::NEG));
+          else vmu = xs[u];
+          const bool hit = um < 0 && vmu == tm;
+          if (hit) {
+            um = u;
+            if constexpr (TMA) qm = q[u];
+            else qm.x = __float_as_uint(xs[u]);
+          } else {
+            sec = fmaxf(sec, vmu);
+          }
+        }
+        float x[VEC];
+        if constexpr (TMA) Vec16<T>::unpack(qm, x);
+        else x[0] = __uint_as_float(qm.x);
+#pragma unroll
+        for (int e2 = 0; e2 < VEC; ++e2) {
+          const bool hit = em < 0 && x[e2] == tm;
+          if (hit) em = e2;
+          else sec = fmaxf(sec, x[e2]);
+        }
+        const u32 so = sec > -INFINITY ? ord_f32(sec) : 0u;
+        const bool known = um >= 0 && em >= 0 && tm != 0.0f && sec != 0.0f && so < 0xffffffe0u;
+        const u32 desc = known ? (((so >> 5) + 1u) << 5) | static_cast<u32>(um * VEC + em) : 0xffffffffu;
+        const int pos = atomicAdd(&sh.qcnt[slot], 1);
+        if (pos < QSEG) {
+          sh.q[slot][pos] = (static_cast<u64>(tmo) << 32) | static_cast<u32>(ch.v0 + tid * VEC);
+          sh.qd[slot][pos] = desc;
+        }
+      }
       // online log-sum-exp in the log2 domain: l = sum 2^(x*log2e - M)
       if (tm > m) {
         const float Mn = tm * LOG2E_F;
@@ -538,24 +605,6 @@ __device__ void consume(const BsArgs& a, BsShared& sh, int64_t e0, int64_t e1) {
 #pragma unroll
           for (int u = 0; u + w < BS_U; u += 2 * w) acc[u] += acc[u + w];
         l += acc[0];
-      }
-      // the threshold: each warp seeds it at the segment's first chunk with the K-th best
-      // of its lane maxima; one warp per chunk raises it from the queue once QSTEP more
-      // tiles have been queued
-      u32 thr_o = *reinterpret_cast<volatile u32*>(&sh.thr[slot]);
-      const u32 tmo = tm > -INFINITY ? ord_f32(tm) : 0u;
-      if (!seeded) {
-        // every consumer warp is at the segment's first chunk: the threshold starts at
-        // the best of the warps' seeds, so only a few tiles of this chunk are queued
-        seeded = true;
-        const u32 seed = warp_kth_u32(tmo, K, lane);
-        if (lane == 0 && seed > thr_o) atomicMax(&sh.thr[slot], seed);
-        named_sync(BAR_CONSUMERS, BS_NC);
-        thr_o = *reinterpret_cast<volatile u32*>(&sh.thr[slot]);
-      }
-      if (tmo != 0u && tmo >= thr_o) {
-        const int pos = atomicAdd(&sh.qcnt[slot], 1);
-        if (pos < QSEG) sh.q[slot][pos] = (static_cast<u64>(tmo) << 32) | static_cast<u32>(ch.v0 + tid * VEC);
       }
       if (warp == (c & (BS_NCW - 1))) {
         const int nq = __shfl_sync(FULL, *reinterpret_cast<volatile int*>(&sh.qcnt[slot]), 0);
