@@ -175,25 +175,15 @@ __global__ void __launch_bounds__(REMAP_NT) kv_paged_remap_kernel(const PagedArg
   int32_t* rc0 = rc + S;               // [S] counts before
   int32_t* stk = rc0 + S;              // [S]
   __shared__ int nold[WMAX], par[WMAX], nnew[WMAX], tail[WMAX];
-  __shared__ int top, any_live;
+  __shared__ int top, any_live, n_tasks;
+  __shared__ int4 task[WMAX];
   const int tid = threadIdx.x;
 
-  if (tid == 0) any_live = 0;
-  __syncthreads();
+  // one round of loads: everything the sentence's remap reads (a finished sentence's
+  // state is read and left as it is)
   if (tid < W) {
     nold[tid] = a.nblk[r0 + tid];
     par[tid] = __ldg(bi + r0 + tid);
-    if (par[tid] >= 0) {
-      if (par[tid] < r0 || par[tid] >= r0 + W) set_status(a.status, VBS_EINVAL);
-      atomicOr(&any_live, 1);
-    }
-  }
-  __syncthreads();
-  if (!any_live) {
-    if (tid == 0) {
-      // a finished sentence: nothing moves, nothing is copied
-    }
-    return;
   }
   for (int i = tid; i < W * MB; i += REMAP_NT) old[i] = a.table[static_cast<int64_t>(r0) * MB + i];
   for (int j = tid; j < S; j += REMAP_NT) {
@@ -201,9 +191,25 @@ __global__ void __launch_bounds__(REMAP_NT) kv_paged_remap_kernel(const PagedArg
     rc0[j] = rc[j];
     stk[j] = a.stack[static_cast<int64_t>(b) * S + j];
   }
-  if (tid == 0) top = a.top[b];
-  if (tid < W && (par[tid] < r0 || par[tid] >= r0 + W)) par[tid] = -1;
+  if (tid == 0) {
+    top = a.top[b];
+    n_tasks = 0;
+  }
   __syncthreads();
+  if (tid == 0) {
+    int live = 0;
+    for (int w = 0; w < W; ++w) {
+      if (par[w] < 0) continue;
+      live = 1;
+      if (par[w] < r0 || par[w] >= r0 + W) {
+        set_status(a.status, VBS_EINVAL);
+        par[w] = -1;
+      }
+    }
+    any_live = live;
+  }
+  __syncthreads();
+  if (!any_live) return;                            // a finished sentence: nothing moves
 
   // new references first, then drop the old ones: a block shared by parent and
   // child never reaches zero in between
@@ -268,12 +274,15 @@ __global__ void __launch_bounds__(REMAP_NT) kv_paged_remap_kernel(const PagedArg
         rc[nb - b * S] = 1;
         rc[blk - b * S] -= 1;
         tail[w] = nb;
-        const int slot = atomicAdd(a.task_count, 1);
-        a.tasks[slot] = make_int4(blk, nb, fill, 0);
-        atomicAdd(a.cow_slots, static_cast<unsigned long long>(fill) * (a.L * 2 * a.H));
+        task[n_tasks++] = make_int4(blk, nb, fill, 0);
       } else {
         set_status(a.status, VBS_EINVAL);                 // the table does not match t_valid
       }
+    }
+    if (n_tasks) {                                        // one reservation for the sentence's copies
+      const int base = atomicAdd(a.task_count, n_tasks);
+      for (int q = 0; q < n_tasks; ++q) a.tasks[base + q] = task[q];
+      atomicAdd(a.cow_slots, static_cast<unsigned long long>(n_tasks) * fill * (a.L * 2 * a.H));
     }
   }
   __syncthreads();
