@@ -941,6 +941,10 @@ __global__ void __launch_bounds__(BS_NT, 1) bs_cluster_kernel(const BsArgs a) {
   }
   for (int i = threadIdx.x; i < NSLOT * QSEG; i += BS_NT) (&sh.q[0][0])[i] = 0ull;
   __syncthreads();
+  // launched as a programmatic dependent: the set-up above overlaps the previous kernel's
+  // tail; every global access comes after it has completed
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if ((threadIdx.x >> 5) == BS_NCW) {
     if constexpr (TMA) {
       if ((threadIdx.x & 31) == 0) produce<T>(a, sh, e0, e1);
@@ -1394,13 +1398,15 @@ static int launch_cluster(const BsArgs& a, cudaStream_t s) {
   cfg.blockDim = dim3(BS_NT);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = a.cluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, bs_cluster_kernel<T, TMA>, a) == cudaSuccess ? VBS_OK : VBS_ECUDA;
 }
 

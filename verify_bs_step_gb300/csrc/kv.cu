@@ -165,6 +165,23 @@ int launch_kv_naive(const KvGeom& g, const void* src, void* dst, const int32_t* 
 
 constexpr int REMAP_NT = 256;
 
+// Launch with programmatic stream serialization: the kernel may be scheduled while its
+// predecessor in the stream finishes; it calls griddepcontrol.wait before touching memory.
+template <typename... KArgs, typename... Args>
+static int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...) == cudaSuccess ? VBS_OK : VBS_ECUDA;
+}
+
 __global__ void __launch_bounds__(REMAP_NT) kv_paged_remap_kernel(const PagedArgs a, const int32_t* bi,
                                                                   int t_valid) {
   extern __shared__ int32_t rs[];
@@ -178,6 +195,10 @@ __global__ void __launch_bounds__(REMAP_NT) kv_paged_remap_kernel(const PagedArg
   __shared__ int top, any_live, n_tasks;
   __shared__ int4 task[WMAX];
   const int tid = threadIdx.x;
+  // launched as a programmatic dependent of the beam step: wait for it (and everything
+  // before it) before the first global access
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // one round of loads: everything the sentence's remap reads (a finished sentence's
   // state is read and left as it is)
@@ -313,8 +334,7 @@ int launch_kv_paged_remap(const PagedArgs& a, const int32_t* beam_idx, int t_val
     cudaFuncSetAttribute(kv_paged_remap_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     attr = smem;
   }
-  kv_paged_remap_kernel<<<a.B, REMAP_NT, smem, s>>>(a, beam_idx, t_valid);
-  return cudaGetLastError() == cudaSuccess ? VBS_OK : VBS_ECUDA;
+  return launch_pdl(kv_paged_remap_kernel, dim3(a.B), dim3(REMAP_NT), smem, s, a, beam_idx, t_valid);
 }
 
 // copy-on-write: task q copies the filled slots of every (l, kv, h) run of a block
@@ -347,6 +367,8 @@ __device__ __forceinline__ void st_stream16(void* p, const uint4& v) {
 }
 
 __global__ void __launch_bounds__(COW_NT) kv_cow_vec_kernel(CowMap map, int32_t* task_count, int32_t* cow_ticket) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");   // the remap's tasks
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int64_t n_items = static_cast<int64_t>(*task_count) * map.n_runs;
   const int lane = threadIdx.x & 31;
   const int64_t nw = static_cast<int64_t>(gridDim.x) * (COW_NT / 32);
@@ -382,6 +404,8 @@ __global__ void __launch_bounds__(COW_NT) kv_cow_vec_kernel(CowMap map, int32_t*
 }
 
 __global__ void kv_cow_plain_kernel(CowMap map, int32_t* task_count, int32_t* cow_ticket) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int64_t n_items = static_cast<int64_t>(*task_count) * map.n_runs;
   for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
     const char* s;
@@ -404,12 +428,11 @@ int launch_kv_paged_cow(const PagedArgs& a, bool bulk_ok, int num_sms, cudaStrea
   const int n_runs = a.L * 2 * a.H;
   const int64_t run_bytes = static_cast<int64_t>(a.block) * a.slot_bytes;
   CowMap m{a.pool, a.tasks, n_runs, a.block_bytes, run_bytes, a.slot_bytes};
-  if (bulk_ok) {
-    kv_cow_vec_kernel<<<num_sms * COW_CTAS_PER_SM, COW_NT, 0, s>>>(m, a.task_count, a.cow_ticket);
-  } else {
-    kv_cow_plain_kernel<<<num_sms * KV_CTAS_PER_SM, 256, 0, s>>>(m, a.task_count, a.cow_ticket);
-  }
-  return cudaGetLastError() == cudaSuccess ? VBS_OK : VBS_ECUDA;
+  if (bulk_ok)
+    return launch_pdl(kv_cow_vec_kernel, dim3(num_sms * COW_CTAS_PER_SM), dim3(COW_NT), 0, s, m, a.task_count,
+                      a.cow_ticket);
+  return launch_pdl(kv_cow_plain_kernel, dim3(num_sms * KV_CTAS_PER_SM), dim3(256), 0, s, m, a.task_count,
+                    a.cow_ticket);
 }
 
 }  // namespace vbs
