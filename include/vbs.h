@@ -256,6 +256,25 @@ int kv_paged_prepare(vbs_pkv* pkv, int t_write);
  * reported by kv_paged_status().
  */
 int kv_paged_reorder(vbs_pkv* pkv, const int32_t* beam_idx, int t_valid);
+/*
+ * One beam step (bs_step, same arguments and outputs) followed by the remap
+ * half of kv_paged_reorder(pkv, beam_idx, t_valid): the table, counts and free
+ * stacks are updated and the copy-on-write tasks recorded, but nothing is
+ * copied until kv_paged_copy(pkv).  bs_step_paged + kv_paged_copy has the
+ * effect of bs_step + kv_paged_reorder ([LM] §9.2.2: the cache follows the
+ * step's beam_idx).  When the beam-search context runs one cluster of CTAs per
+ * sentence, the remap runs inside the beam-step kernel after each sentence's
+ * merge, on the beam_idx it has just written (one launch instead of two);
+ * otherwise it is a second launch.  pkv must describe the same batch and W and
+ * use the same stream as ctx.  No pages' counterpart as one call: the pages
+ * describe the two operations separately.
+ * Errors: those of bs_step and kv_paged_reorder; VBS_EINVAL for a pkv of
+ * another batch, W or stream.  Device-side remap errors go to kv_paged_status().
+ */
+int bs_step_paged(vbs_bs* ctx, const void* logits, int64_t ld, float* scores, int32_t* seqs, int32_t* beam_idx,
+                  int32_t* tokens, int32_t* all_done, vbs_pkv* pkv, int t_valid);
+/* The copy-on-write tasks recorded by bs_step_paged (one launch; none pending: no copy). */
+int kv_paged_copy(vbs_pkv* pkv);
 /* The device block table [R][max_blocks] and its row stride. */
 int kv_paged_table(vbs_pkv* pkv, const int32_t** table, int* max_blocks);
 /* Copy the reference counts [num_blocks] and per-row block counts [R] to device buffers (either may be NULL). */

@@ -47,6 +47,8 @@ SIGNATURES = {
     "kv_paged_prefill": (_c_int, [_vp, _c_int]),
     "kv_paged_prepare": (_c_int, [_vp, _c_int]),
     "kv_paged_reorder": (_c_int, [_vp, _vp, _c_int]),
+    "bs_step_paged": (_c_int, [_vp, _vp, _c_i64, _vp, _vp, _vp, _vp, _vp, _vp, _c_int]),
+    "kv_paged_copy": (_c_int, [_vp]),
     "kv_paged_table": (_c_int, [_vp, _pp, ctypes.POINTER(_c_int)]),
     "kv_paged_counts": (_c_int, [_vp, _vp, _vp]),
     "kv_paged_copy_table": (_c_int, [_vp, _vp]),
@@ -149,6 +151,19 @@ class BeamSearch:
         _check(lib().bs_step(self.ctx, _dev_ptr(logits, "logits"), logits.stride(0), _vp(self.scores.data_ptr()),
                              _vp(self.seqs.data_ptr()), _vp(self.beam_idx.data_ptr()),
                              _vp(self.tokens.data_ptr()), _vp(self.all_done.data_ptr())), "bs_step")
+        return self.beam_idx, self.tokens, self.scores
+
+    def step_paged(self, logits: torch.Tensor, kv: "PagedKV", t_valid: int):
+        """step() plus the table remap of kv.reorder(beam_idx, t_valid); the copy-on-write
+        runs at kv.copy().  Returns (beam_idx, tokens, scores) views."""
+        if logits.dim() != 2 or logits.shape[0] != self.R or logits.shape[1] != self.V or logits.stride(1) != 1:
+            raise ValueError(f"logits must be [{self.R}, {self.V}] with unit stride along V")
+        if logits.dtype != self.dtype:
+            raise ValueError(f"logits must be {self.dtype}")
+        _check(lib().bs_step_paged(self.ctx, _dev_ptr(logits, "logits"), logits.stride(0),
+                                   _vp(self.scores.data_ptr()), _vp(self.seqs.data_ptr()),
+                                   _vp(self.beam_idx.data_ptr()), _vp(self.tokens.data_ptr()),
+                                   _vp(self.all_done.data_ptr()), kv.ctx, t_valid), "bs_step_paged")
         return self.beam_idx, self.tokens, self.scores
 
     def finalize(self):
@@ -281,6 +296,10 @@ class PagedKV:
     def reorder(self, beam_idx: torch.Tensor, t_valid: int):
         _check(lib().kv_paged_reorder(self.ctx, _dev_ptr(beam_idx, "beam_idx", torch.int32), t_valid),
                "kv_paged_reorder")
+
+    def copy(self):
+        """Run the copy-on-write tasks that BeamSearch.step_paged recorded."""
+        _check(lib().kv_paged_copy(self.ctx), "kv_paged_copy")
 
     def save(self):
         """Snapshot the allocator state on the device (no host round trip)."""

@@ -217,14 +217,15 @@ VBS_EXPORT int bs_reset(vbs_bs* c, float* scores, int32_t* seqs) {
   return VBS_OK;
 }
 
-VBS_EXPORT int bs_step(vbs_bs* c, const void* logits, int64_t ld, float* scores, int32_t* seqs,
-                       int32_t* beam_idx, int32_t* tokens, int32_t* all_done) {
+// The kernel arguments of one step (validated), shared by bs_step and bs_step_paged.
+static int step_args(vbs_bs* c, const void* logits, int64_t ld, float* scores, int32_t* seqs, int32_t* beam_idx,
+                     int32_t* tokens, int32_t* all_done, vbs::BsArgs& a, bool& vec_ok) {
   if (!c || !logits || !scores || !beam_idx || !tokens) return VBS_EINVAL;
   if (ld < c->a.V) return VBS_EINVAL;
   if (!c->reset_done || c->step >= c->a.max_len) return VBS_ESTATE;
   int32_t* sq = seqs ? seqs : c->own_seqs;
   if (sq != c->seqs_bound) return VBS_ESTATE;
-  vbs::BsArgs a = c->a;
+  a = c->a;
   a.logits = logits;
   a.ld = ld;
   a.scores = scores;
@@ -238,10 +239,20 @@ VBS_EXPORT int bs_step(vbs_bs* c, const void* logits, int64_t ld, float* scores,
                                                                    : a.lp_t;
   a.lp_tf = static_cast<float>(a.lp_t);
   a.lp_boundf = static_cast<float>(a.lp_bound);
+  a.kv_fuse = 0;
   const int es = a.dtype == VBS_BF16 ? 2 : 4;
   const int VEC = 16 / es;
-  const bool vec_ok = aligned16(logits) && (ld * es) % 16 == 0 && a.V % VEC == 0;
-  int st = vbs::launch_bs_step(a, c->grid, vec_ok, c->stream);
+  vec_ok = aligned16(logits) && (ld * es) % 16 == 0 && a.V % VEC == 0;
+  return VBS_OK;
+}
+
+VBS_EXPORT int bs_step(vbs_bs* c, const void* logits, int64_t ld, float* scores, int32_t* seqs,
+                       int32_t* beam_idx, int32_t* tokens, int32_t* all_done) {
+  vbs::BsArgs a;
+  bool vec_ok = false;
+  int st = step_args(c, logits, ld, scores, seqs, beam_idx, tokens, all_done, a, vec_ok);
+  if (st != VBS_OK) return st;
+  st = vbs::launch_bs_step(a, c->grid, vec_ok, c->stream);
   if (st != VBS_OK) return st;
   c->step += 1;
   return VBS_OK;
@@ -502,6 +513,36 @@ VBS_EXPORT int kv_paged_prepare(vbs_pkv* c, int t_write) {
 VBS_EXPORT int kv_paged_reorder(vbs_pkv* c, const int32_t* beam_idx, int t_valid) {
   if (!c || !beam_idx) return VBS_EINVAL;
   return paged_run(c, beam_idx, t_valid);
+}
+
+VBS_EXPORT int bs_step_paged(vbs_bs* c, const void* logits, int64_t ld, float* scores, int32_t* seqs,
+                             int32_t* beam_idx, int32_t* tokens, int32_t* all_done, vbs_pkv* kv, int t_valid) {
+  if (!kv) return VBS_EINVAL;
+  vbs::BsArgs a;
+  bool vec_ok = false;
+  int st = step_args(c, logits, ld, scores, seqs, beam_idx, tokens, all_done, a, vec_ok);
+  if (st != VBS_OK) return st;
+  if (kv->a.B != a.B || kv->a.W != a.W || kv->stream != c->stream) return VBS_EINVAL;
+  const int64_t need = static_cast<int64_t>(t_valid) / kv->a.block + 1;
+  if (t_valid < 0 || need > kv->a.MB) return VBS_EINVAL;
+  if (vbs::bs_can_fuse_remap(a, kv->a)) {
+    a.kv_fuse = 1;
+    a.kv_t = t_valid;
+    a.kv = kv->a;
+    st = vbs::launch_bs_step(a, c->grid, vec_ok, c->stream);
+  } else {
+    st = vbs::launch_bs_step(a, c->grid, vec_ok, c->stream);
+    if (st == VBS_OK) st = vbs::launch_kv_paged_remap(kv->a, beam_idx, t_valid, kv->stream);
+  }
+  if (st != VBS_OK) return st;
+  c->step += 1;
+  return VBS_OK;
+}
+
+VBS_EXPORT int kv_paged_copy(vbs_pkv* c) {
+  if (!c) return VBS_EINVAL;
+  const bool bulk_ok = c->a.slot_bytes % 16 == 0 && aligned16(c->a.pool);
+  return vbs::launch_kv_paged_cow(c->a, bulk_ok, num_sms(), c->stream);
 }
 
 VBS_EXPORT int kv_paged_table(vbs_pkv* c, const int32_t** table, int* max_blocks) {

@@ -11,6 +11,24 @@ constexpr int KMAX = 2 * WMAX;    // candidates kept per row (2W)
 constexpr int PART_KEYS = 256;    // keys one row merge can hold (partials x K)
 constexpr int CAND_CAP = 288;     // candidate buffer per warp: K + one 32-lane x 8-element vector
 
+// Paged KV cache: one sentence's blocks live in [b*S, (b+1)*S) of the pool.
+struct PagedArgs {
+  int B, W, S, MB, block, L, H;
+  int64_t block_bytes;            // bytes of one pool block
+  int64_t slot_bytes;             // bytes of one position within one (l, kv, h) run
+  char* pool;
+  int32_t* table;                 // [R, MB]
+  int32_t* nblk;                  // [R]
+  int32_t* refcnt;                // [B*S]
+  int32_t* stack;                 // [B*S]
+  int32_t* top;                   // [B]
+  int4* tasks;                    // [R] (src block, dst block, filled slots, -)
+  int32_t* task_count;
+  int32_t* cow_ticket;
+  unsigned long long* cow_slots;  // filled slots copied, summed (x L*2*H runs)
+  int* status;
+};
+
 struct BsArgs {
   const void* logits;
   int64_t ld;
@@ -51,9 +69,14 @@ struct BsArgs {
   int* fin_next;
   double* fin_worst;
   int* status;
+  // cluster mode: the paged KV remap of the step, fused after the sentence merge (kv_fuse != 0)
+  int kv_fuse;
+  int kv_t;                       // t_valid of the remap
+  PagedArgs kv;
 };
 
 int launch_bs_step(const BsArgs& a, int grid, bool vector_ok, cudaStream_t s);
+bool bs_can_fuse_remap(const BsArgs& a, const PagedArgs& kv);
 int launch_bs_reset(const BsArgs& a, cudaStream_t s);
 int launch_bs_finalize(const BsArgs& a, const float* scores, const int32_t* seqs, int32_t* out_seqs,
                        int32_t* out_len, float* out_score, cudaStream_t s);
@@ -75,22 +98,6 @@ struct KvGeom {
 int launch_kv_naive(const KvGeom& g, const void* src, void* dst, const int32_t* beam_idx, bool bulk_ok,
                     int elem_bytes, int* status, int num_sms, cudaStream_t s);
 
-struct PagedArgs {
-  int B, W, S, MB, block, L, H;
-  int64_t block_bytes;            // bytes of one pool block
-  int64_t slot_bytes;             // bytes of one position within one (l, kv, h) run
-  char* pool;
-  int32_t* table;                 // [R, MB]
-  int32_t* nblk;                  // [R]
-  int32_t* refcnt;                // [B*S]
-  int32_t* stack;                 // [B*S]
-  int32_t* top;                   // [B]
-  int4* tasks;                    // [R] (src block, dst block, filled slots, -)
-  int32_t* task_count;
-  int32_t* cow_ticket;
-  unsigned long long* cow_slots;  // filled slots copied, summed (x L*2*H runs)
-  int* status;
-};
 int launch_kv_paged_remap(const PagedArgs& a, const int32_t* beam_idx, int t_valid, cudaStream_t s);
 int launch_kv_paged_cow(const PagedArgs& a, bool bulk_ok, int num_sms, cudaStream_t s);
 

@@ -36,6 +36,7 @@
 
 #include "common.cuh"
 #include "bs_internal.h"
+#include "kv_remap.cuh"
 
 namespace vbs {
 
@@ -150,6 +151,14 @@ struct BsShared {                              // the stream kernel
 };
 
 static_assert(sizeof(BsShared) <= 232448, "the stream kernel's shared memory fits one SM");
+constexpr int REMAP_SH_BYTES = (static_cast<int>(sizeof(RemapShared)) + 15) / 16 * 16;
+
+// The cluster kernel can run a sentence's paged KV remap after its merge when the remap's
+// shared state fits in the (then idle) ring.
+bool bs_can_fuse_remap(const BsArgs& a, const PagedArgs& kv) {
+  return a.cluster != 0 && kv.B == a.B && kv.W == a.W &&
+         REMAP_SH_BYTES + remap_scratch_ints(kv) * 4 <= static_cast<int64_t>(sizeof(BsShared::ring));
+}
 
 struct MergeShared {                           // the merge kernel
   u64 rowscratch[WMAX * PART_KEYS];            // the rows' partial lists
@@ -946,8 +955,19 @@ __global__ void __launch_bounds__(BS_NT, 1) bs_cluster_kernel(const BsArgs a) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if ((threadIdx.x >> 5) == BS_NCW) {
-    if constexpr (TMA) {
-      if ((threadIdx.x & 31) == 0) produce<T>(a, sh, e0, e1);
+    const int lane = threadIdx.x & 31;
+    if (TMA && lane == 0) {
+      produce<T>(a, sh, e0, e1);
+    } else if (a.kv_fuse && c == 0) {
+      // the idle producer lanes pull the sentence's KV block state into L2 for the
+      // remap that follows the merge
+      const PagedArgs& kv = a.kv;
+      const int r0 = b * a.W;
+      prefetch_l2(kv.table + static_cast<int64_t>(r0) * kv.MB, static_cast<int64_t>(a.W) * kv.MB * 4, lane - 1, 31);
+      prefetch_l2(kv.refcnt + static_cast<int64_t>(b) * kv.S, static_cast<int64_t>(kv.S) * 4, lane - 1, 31);
+      prefetch_l2(kv.stack + static_cast<int64_t>(b) * kv.S, static_cast<int64_t>(kv.S) * 4, lane - 1, 31);
+      prefetch_l2(kv.nblk + r0, static_cast<int64_t>(a.W) * 4, lane - 1, 31);
+      prefetch_l2(kv.top + b, 4, lane - 1, 31);
     }
   } else {
     if (c == 0 && threadIdx.x < 32) cluster_prefetch(a, sh, b, threadIdx.x);
@@ -957,6 +977,13 @@ __global__ void __launch_bounds__(BS_NT, 1) bs_cluster_kernel(const BsArgs a) {
   cooperative_groups::this_cluster().sync();       // every CTA's row results are in its shared memory
   if (c == 0 && threadIdx.x < 32) cluster_merge_sentence(a, sh, b, threadIdx.x);
   cooperative_groups::this_cluster().sync();       // keep them readable until the merge is done
+  if (a.kv_fuse && c == 0) {
+    // the paged KV remap of the sentence, on the step's beam_idx just written; the ring is
+    // free now and holds its shared state
+    RemapShared& rsh = *reinterpret_cast<RemapShared*>(&sh.ring[0][0]);
+    int32_t* rs = reinterpret_cast<int32_t*>(&sh.ring[0][0] + REMAP_SH_BYTES);
+    paged_remap_sentence<BS_NT>(a.kv, b, a.beam_idx, a.kv_t, rs, rsh);
+  }
 }
 
 // ---------------------------------------------------------------------------------------

@@ -48,6 +48,14 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
   return r;
 }
 
+// Prefetch [p, p + bytes) into L2, one 128-byte line per call, lines i = lane, lane + nl, ...
+__device__ __forceinline__ void prefetch_l2(const void* p, int64_t bytes, int lane, int nl) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(p) & ~static_cast<uintptr_t>(127);
+  const uintptr_t a1 = reinterpret_cast<uintptr_t>(p) + static_cast<uintptr_t>(bytes);
+  for (uintptr_t q = a0 + static_cast<uintptr_t>(lane) * 128; q < a1; q += static_cast<uintptr_t>(nl) * 128)
+    asm volatile("prefetch.global.L2 [%0];" :: "l"(q));
+}
+
 // Unpack one 16-byte vector into VEC floats (8 bf16 or 4 fp32).
 template <typename T> struct Vec16;
 template <> struct Vec16<bf16_t> {

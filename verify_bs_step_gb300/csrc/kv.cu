@@ -13,11 +13,12 @@
 // them with cp.async.bulk shared->global stores (bulk groups).  The remap of
 // the paged table is sentence-local (blocks are never shared across
 // sentences), so it runs one CTA per sentence on shared-memory copies of the
-// sentence's table rows, reference counts and free stack, with no global
-// atomics and a deterministic allocation order.
+// sentence's table rows, reference counts and free stack, with one global
+// atomic per sentence and a deterministic allocation order (kv_remap.cuh).
 
 #include "common.cuh"
 #include "bs_internal.h"
+#include "kv_remap.cuh"
 
 namespace vbs {
 
@@ -185,149 +186,16 @@ static int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sm
 __global__ void __launch_bounds__(REMAP_NT) kv_paged_remap_kernel(const PagedArgs a, const int32_t* bi,
                                                                   int t_valid) {
   extern __shared__ int32_t rs[];
-  const int b = blockIdx.x, W = a.W, S = a.S, MB = a.MB;
-  const int r0 = b * W;
-  int32_t* old = rs;                   // [W][MB]
-  int32_t* rc = old + W * MB;          // [S] counts now
-  int32_t* rc0 = rc + S;               // [S] counts before
-  int32_t* stk = rc0 + S;              // [S]
-  __shared__ int nold[WMAX], par[WMAX], nnew[WMAX], tail[WMAX];
-  __shared__ int top, any_live, n_tasks;
-  __shared__ int4 task[WMAX];
-  const int tid = threadIdx.x;
+  __shared__ RemapShared sh;
   // launched as a programmatic dependent of the beam step: wait for it (and everything
   // before it) before the first global access
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-
-  // one round of loads: everything the sentence's remap reads (a finished sentence's
-  // state is read and left as it is)
-  if (tid < W) {
-    nold[tid] = a.nblk[r0 + tid];
-    par[tid] = __ldg(bi + r0 + tid);
-  }
-  for (int i = tid; i < W * MB; i += REMAP_NT) old[i] = a.table[static_cast<int64_t>(r0) * MB + i];
-  for (int j = tid; j < S; j += REMAP_NT) {
-    rc[j] = a.refcnt[static_cast<int64_t>(b) * S + j];
-    rc0[j] = rc[j];
-    stk[j] = a.stack[static_cast<int64_t>(b) * S + j];
-  }
-  if (tid == 0) {
-    top = a.top[b];
-    n_tasks = 0;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    int live = 0;
-    for (int w = 0; w < W; ++w) {
-      if (par[w] < 0) continue;
-      live = 1;
-      if (par[w] < r0 || par[w] >= r0 + W) {
-        set_status(a.status, VBS_EINVAL);
-        par[w] = -1;
-      }
-    }
-    any_live = live;
-  }
-  __syncthreads();
-  if (!any_live) return;                            // a finished sentence: nothing moves
-
-  // new references first, then drop the old ones: a block shared by parent and
-  // child never reaches zero in between
-  for (int i = tid; i < W * MB; i += REMAP_NT) {
-    const int w = i / MB, s = i - w * MB;
-    const int p = par[w];
-    if (p >= 0 && s < nold[p - r0]) {
-      const int blk = old[(p - r0) * MB + s] - b * S;
-      if (blk >= 0 && blk < S) atomicAdd(&rc[blk], 1);
-      else set_status(a.status, VBS_EINVAL);
-    }
-  }
-  __syncthreads();
-  for (int i = tid; i < W * MB; i += REMAP_NT) {
-    const int w = i / MB, s = i - w * MB;
-    if (par[w] >= 0 && s < nold[w]) {
-      const int blk = old[w * MB + s] - b * S;
-      if (blk >= 0 && blk < S) atomicSub(&rc[blk], 1);
-    }
-  }
-  __syncthreads();
-  // freed blocks go back on the stack in ascending id order
-  if (tid < 32) {
-    for (int j0 = 0; j0 < S; j0 += 32) {
-      const int j = j0 + tid;
-      const bool freed = j < S && rc0[j] > 0 && rc[j] == 0;
-      const u32 m = __ballot_sync(FULL, freed);
-      const int pos = top + __popc(m & ((1u << tid) - 1u));
-      if (freed && pos < S) stk[pos] = b * S + j;
-      __syncwarp();
-      if (tid == 0) top = min(S, top + __popc(m));
-      __syncwarp();
-    }
-  }
-  __syncthreads();
-
-  // make the block holding position t_valid exclusive to each live row
-  if (tid == 0) {
-    const int i = t_valid / a.block, fill = t_valid % a.block;
-    int kept[WMAX];
-    int n_kept = 0;
-    for (int w = 0; w < W; ++w) {
-      tail[w] = -1;
-      const int p = par[w];
-      if (p < 0) { nnew[w] = nold[w]; continue; }
-      const int n = nold[p - r0];
-      nnew[w] = n;
-      if (n == i) {                                       // a fresh block, nothing to copy
-        if (top == 0) { set_status(a.status, VBS_ENOMEM); continue; }
-        const int nb = stk[--top];
-        rc[nb - b * S] = 1;
-        tail[w] = nb;
-        nnew[w] = i + 1;
-      } else if (n == i + 1) {
-        const int blk = old[(p - r0) * MB + i];
-        if (rc[blk - b * S] == 1) continue;
-        bool is_kept = false;
-        for (int q = 0; q < n_kept; ++q) is_kept |= kept[q] == blk;
-        if (!is_kept) { kept[n_kept++] = blk; continue; }  // the lowest row keeps the shared block
-        if (top == 0) { set_status(a.status, VBS_ENOMEM); continue; }
-        const int nb = stk[--top];
-        rc[nb - b * S] = 1;
-        rc[blk - b * S] -= 1;
-        tail[w] = nb;
-        task[n_tasks++] = make_int4(blk, nb, fill, 0);
-      } else {
-        set_status(a.status, VBS_EINVAL);                 // the table does not match t_valid
-      }
-    }
-    if (n_tasks) {                                        // one reservation for the sentence's copies
-      const int base = atomicAdd(a.task_count, n_tasks);
-      for (int q = 0; q < n_tasks; ++q) a.tasks[base + q] = task[q];
-      atomicAdd(a.cow_slots, static_cast<unsigned long long>(n_tasks) * fill * (a.L * 2 * a.H));
-    }
-  }
-  __syncthreads();
-
-  // write back
-  const int ti = t_valid / a.block;
-  for (int i = tid; i < W * MB; i += REMAP_NT) {
-    const int w = i / MB, s = i - w * MB;
-    const int p = par[w];
-    if (p < 0) continue;
-    int v = s < nold[p - r0] ? old[(p - r0) * MB + s] : -1;
-    if (s == ti && tail[w] >= 0) v = tail[w];
-    if (s < nnew[w]) a.table[static_cast<int64_t>(r0 + w) * MB + s] = v;
-  }
-  if (tid < W) a.nblk[r0 + tid] = nnew[tid];
-  for (int j = tid; j < S; j += REMAP_NT) {
-    a.refcnt[static_cast<int64_t>(b) * S + j] = rc[j];
-    a.stack[static_cast<int64_t>(b) * S + j] = stk[j];
-  }
-  if (tid == 0) a.top[b] = top;
+  paged_remap_sentence<REMAP_NT>(a, blockIdx.x, bi, t_valid, rs, sh);
 }
 
 int launch_kv_paged_remap(const PagedArgs& a, const int32_t* beam_idx, int t_valid, cudaStream_t s) {
-  const size_t smem = (static_cast<size_t>(a.W) * a.MB + 3 * static_cast<size_t>(a.S)) * sizeof(int32_t);
+  const size_t smem = static_cast<size_t>(remap_scratch_ints(a)) * sizeof(int32_t);
   if (smem > 200 * 1024) return VBS_EINVAL;
   static size_t attr = 0;
   if (smem > 48 * 1024 && smem > attr) {

@@ -1,0 +1,172 @@
+// The paged KV remap of one sentence, run by one CTA of NT threads: shared by the
+// standalone remap kernel and the beam-step kernel that fuses it after its merge.
+//
+// What is computed follows "9.2 贪心搜索与束搜索：确定性与近似搜索" §9.2.2 (the
+// cache paragraph: row r continues from the cache of its parent beam_idx[r]; a
+// paged cache rewrites block-table entries and copies only when a shared block is
+// written).  The remap is sentence-local (blocks are never shared across
+// sentences): the sentence's table rows, reference counts and free stack are
+// loaded into shared memory in one round, new references are counted before old
+// ones are dropped (a block shared by parent and child never reaches zero in
+// between), freed blocks return to the stack in ascending id order, thread 0 makes
+// the block holding position t_valid exclusive to every live row in row order (a
+// fresh block, or a copy-on-write task when it is shared), and the sentence's
+// tasks are reserved with one global atomic.
+#pragma once
+
+#include "common.cuh"
+#include "bs_internal.h"
+
+namespace vbs {
+
+struct RemapShared {
+  int nold[WMAX], par[WMAX], nnew[WMAX], tail[WMAX];
+  int top, any_live, n_tasks;
+  int4 task[WMAX];
+};
+
+// Shared-memory ints the remap needs besides RemapShared.
+__host__ __device__ inline int64_t remap_scratch_ints(const PagedArgs& a) {
+  return static_cast<int64_t>(a.W) * a.MB + 3 * static_cast<int64_t>(a.S);
+}
+
+// Every thread of the CTA calls it (it synchronises the CTA); bi is the step's
+// beam_idx (global rows, -1 for a finished sentence's pads).
+template <int NT>
+__device__ void paged_remap_sentence(const PagedArgs& a, int b, const int32_t* bi, int t_valid, int32_t* rs,
+                                     RemapShared& sh) {
+  const int W = a.W, S = a.S, MB = a.MB;
+  const int r0 = b * W;
+  int32_t* old = rs;                   // [W][MB]
+  int32_t* rc = old + W * MB;          // [S] counts now
+  int32_t* rc0 = rc + S;               // [S] counts before
+  int32_t* stk = rc0 + S;              // [S]
+  const int tid = threadIdx.x;
+
+  // one round of loads: everything the sentence's remap reads (a finished sentence's
+  // state is read and left as it is)
+  if (tid < W) {
+    sh.nold[tid] = a.nblk[r0 + tid];
+    sh.par[tid] = __ldcg(bi + r0 + tid);               // the fused caller wrote it in this kernel
+  }
+  for (int i = tid; i < W * MB; i += NT) old[i] = a.table[static_cast<int64_t>(r0) * MB + i];
+  for (int j = tid; j < S; j += NT) {
+    rc[j] = a.refcnt[static_cast<int64_t>(b) * S + j];
+    rc0[j] = rc[j];
+    stk[j] = a.stack[static_cast<int64_t>(b) * S + j];
+  }
+  if (tid == 0) {
+    sh.top = a.top[b];
+    sh.n_tasks = 0;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int live = 0;
+    for (int w = 0; w < W; ++w) {
+      if (sh.par[w] < 0) continue;
+      live = 1;
+      if (sh.par[w] < r0 || sh.par[w] >= r0 + W) {
+        set_status(a.status, VBS_EINVAL);
+        sh.par[w] = -1;
+      }
+    }
+    sh.any_live = live;
+  }
+  __syncthreads();
+  if (!sh.any_live) return;                            // a finished sentence: nothing moves
+
+  // new references first, then drop the old ones: a block shared by parent and
+  // child never reaches zero in between
+  for (int i = tid; i < W * MB; i += NT) {
+    const int w = i / MB, s = i - w * MB;
+    const int p = sh.par[w];
+    if (p >= 0 && s < sh.nold[p - r0]) {
+      const int blk = old[(p - r0) * MB + s] - b * S;
+      if (blk >= 0 && blk < S) atomicAdd(&rc[blk], 1);
+      else set_status(a.status, VBS_EINVAL);
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < W * MB; i += NT) {
+    const int w = i / MB, s = i - w * MB;
+    if (sh.par[w] >= 0 && s < sh.nold[w]) {
+      const int blk = old[w * MB + s] - b * S;
+      if (blk >= 0 && blk < S) atomicSub(&rc[blk], 1);
+    }
+  }
+  __syncthreads();
+  // freed blocks go back on the stack in ascending id order
+  if (tid < 32) {
+    for (int j0 = 0; j0 < S; j0 += 32) {
+      const int j = j0 + tid;
+      const bool freed = j < S && rc0[j] > 0 && rc[j] == 0;
+      const u32 m = __ballot_sync(FULL, freed);
+      const int pos = sh.top + __popc(m & ((1u << tid) - 1u));
+      if (freed && pos < S) stk[pos] = b * S + j;
+      __syncwarp();
+      if (tid == 0) sh.top = min(S, sh.top + __popc(m));
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+
+  // make the block holding position t_valid exclusive to each live row
+  if (tid == 0) {
+    const int i = t_valid / a.block, fill = t_valid % a.block;
+    int kept[WMAX];
+    int n_kept = 0;
+    for (int w = 0; w < W; ++w) {
+      sh.tail[w] = -1;
+      const int p = sh.par[w];
+      if (p < 0) { sh.nnew[w] = sh.nold[w]; continue; }
+      const int n = sh.nold[p - r0];
+      sh.nnew[w] = n;
+      if (n == i) {                                       // a fresh block, nothing to copy
+        if (sh.top == 0) { set_status(a.status, VBS_ENOMEM); continue; }
+        const int nb = stk[--sh.top];
+        rc[nb - b * S] = 1;
+        sh.tail[w] = nb;
+        sh.nnew[w] = i + 1;
+      } else if (n == i + 1) {
+        const int blk = old[(p - r0) * MB + i];
+        if (rc[blk - b * S] == 1) continue;
+        bool is_kept = false;
+        for (int q = 0; q < n_kept; ++q) is_kept |= kept[q] == blk;
+        if (!is_kept) { kept[n_kept++] = blk; continue; }  // the lowest row keeps the shared block
+        if (sh.top == 0) { set_status(a.status, VBS_ENOMEM); continue; }
+        const int nb = stk[--sh.top];
+        rc[nb - b * S] = 1;
+        rc[blk - b * S] -= 1;
+        sh.tail[w] = nb;
+        sh.task[sh.n_tasks++] = make_int4(blk, nb, fill, 0);
+      } else {
+        set_status(a.status, VBS_EINVAL);                 // the table does not match t_valid
+      }
+    }
+    if (sh.n_tasks) {                                     // one reservation for the sentence's copies
+      const int base = atomicAdd(a.task_count, sh.n_tasks);
+      for (int q = 0; q < sh.n_tasks; ++q) a.tasks[base + q] = sh.task[q];
+      atomicAdd(a.cow_slots, static_cast<unsigned long long>(sh.n_tasks) * fill * (a.L * 2 * a.H));
+    }
+  }
+  __syncthreads();
+
+  // write back
+  const int ti = t_valid / a.block;
+  for (int i = tid; i < W * MB; i += NT) {
+    const int w = i / MB, s = i - w * MB;
+    const int p = sh.par[w];
+    if (p < 0) continue;
+    int v = s < sh.nold[p - r0] ? old[(p - r0) * MB + s] : -1;
+    if (s == ti && sh.tail[w] >= 0) v = sh.tail[w];
+    if (s < sh.nnew[w]) a.table[static_cast<int64_t>(r0 + w) * MB + s] = v;
+  }
+  if (tid < W) a.nblk[r0 + tid] = sh.nnew[tid];
+  for (int j = tid; j < S; j += NT) {
+    a.refcnt[static_cast<int64_t>(b) * S + j] = rc[j];
+    a.stack[static_cast<int64_t>(b) * S + j] = stk[j];
+  }
+  if (tid == 0) a.top[b] = sh.top;
+}
+
+}  // namespace vbs
