@@ -268,8 +268,12 @@ int kv_paged_reorder(vbs_pkv* pkv, const int32_t* beam_idx, int t_valid);
  * otherwise it is a second launch.  pkv must describe the same batch and W and
  * use the same stream as ctx.  No pages' counterpart as one call: the pages
  * describe the two operations separately.
+ * Until kv_paged_copy runs, the recorded copies are pending: another
+ * bs_step_paged, kv_paged_reorder or kv_paged_prepare on pkv returns
+ * VBS_ESTATE (kv_paged_restore and kv_paged_prefill drop pending copies).
  * Errors: those of bs_step and kv_paged_reorder; VBS_EINVAL for a pkv of
- * another batch, W or stream.  Device-side remap errors go to kv_paged_status().
+ * another batch, W or stream; VBS_ESTATE as above.  Device-side remap errors
+ * go to kv_paged_status() (VBS_ESTATE there: more copy tasks than rows).
  */
 int bs_step_paged(vbs_bs* ctx, const void* logits, int64_t ld, float* scores, int32_t* seqs, int32_t* beam_idx,
                   int32_t* tokens, int32_t* all_done, vbs_pkv* pkv, int t_valid);

@@ -110,6 +110,26 @@ def test_fused_llama_shape_two_steps():
     _run_fused(case, L=1, H=1, D=8, P=1000)
 
 
+def test_fused_copies_must_run_before_the_next_remap():
+    import verify_bs_step_gb300 as vbs
+    bs = vbs.BeamSearch(2, 4, 64, eos=3, max_len=4, dtype=torch.float32)
+    pk = vbs.PagedKV(2, 4, 1, 1, 8, blocks_per_sentence=8, max_blocks=4, block=16, dtype=torch.float32)
+    pk.prefill(4)
+    pk.prepare(4)
+    logits = synth.normal_rows(8, 64, 2.0, seed=5).cuda()
+    bs.step_paged(logits, pk, 5)
+    for call in (lambda: bs.step_paged(logits, pk, 6), lambda: pk.reorder(bs.beam_idx, 6), lambda: pk.prepare(6)):
+        with pytest.raises(vbs.VbsError) as e:
+            call()
+        assert e.value.status == vbs.ESTATE
+    pk.copy()
+    bs.step_paged(logits, pk, 6)
+    pk.copy()
+    assert pk.status() == 0 and bs.status() == 0
+    bs.close()
+    pk.close()
+
+
 def test_fused_rejects_a_mismatched_cache():
     import verify_bs_step_gb300 as vbs
     bs = vbs.BeamSearch(2, 4, 64, eos=3, max_len=4, dtype=torch.float32)

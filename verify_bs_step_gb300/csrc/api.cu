@@ -69,6 +69,7 @@ struct vbs_pkv {
   char* state;           // table .. top: one contiguous range of the allocation
   char* saved;           // its copy (kv_paged_save / kv_paged_restore)
   size_t state_bytes;
+  bool copy_pending;     // bs_step_paged recorded copies that kv_paged_copy has not run
 };
 
 VBS_EXPORT const char* vbs_strerror(int status) {
@@ -437,8 +438,7 @@ VBS_EXPORT int kv_paged_init(vbs_pkv** out, const vbs_kv_desc* d, int batch, int
     c->state = reinterpret_cast<char*>(a.table);
     c->state_bytes = state_end;
     a.tasks = cv.take<int4>(R);
-    a.task_count = cv.take<int32_t>(1);
-    a.cow_ticket = cv.take<int32_t>(1);
+    a.task_cap = static_cast<int>(R);
     a.cow_slots = cv.take<unsigned long long>(1);
     a.status = cv.take<int>(1);
     c->identity = cv.take<int32_t>(R);
@@ -475,6 +475,7 @@ VBS_EXPORT int kv_paged_init(vbs_pkv** out, const vbs_kv_desc* d, int batch, int
 }
 
 static int paged_run(vbs_pkv* c, const int32_t* bi, int t_valid) {
+  if (c->copy_pending) return VBS_ESTATE;
   const int64_t need = static_cast<int64_t>(t_valid) / c->a.block + 1;
   if (t_valid < 0 || need > c->a.MB) return VBS_EINVAL;
   int st = vbs::launch_kv_paged_remap(c->a, bi, t_valid, c->stream);
@@ -501,7 +502,9 @@ VBS_EXPORT int kv_paged_prefill(vbs_pkv* c, int P) {
   ok = ok && cudaMemcpyAsync(a.refcnt, refcnt.data(), refcnt.size() * 4, cudaMemcpyHostToDevice, c->stream) == cudaSuccess;
   ok = ok && cudaMemcpyAsync(a.stack, stack.data(), stack.size() * 4, cudaMemcpyHostToDevice, c->stream) == cudaSuccess;
   ok = ok && cudaMemcpyAsync(a.top, top.data(), top.size() * 4, cudaMemcpyHostToDevice, c->stream) == cudaSuccess;
+  ok = ok && cudaMemsetAsync(a.tasks, 0, sizeof(int4) * c->R, c->stream) == cudaSuccess;
   ok = ok && cudaStreamSynchronize(c->stream) == cudaSuccess;
+  c->copy_pending = false;
   return ok ? VBS_OK : VBS_ECUDA;
 }
 
@@ -523,6 +526,7 @@ VBS_EXPORT int bs_step_paged(vbs_bs* c, const void* logits, int64_t ld, float* s
   int st = step_args(c, logits, ld, scores, seqs, beam_idx, tokens, all_done, a, vec_ok);
   if (st != VBS_OK) return st;
   if (kv->a.B != a.B || kv->a.W != a.W || kv->stream != c->stream) return VBS_EINVAL;
+  if (kv->copy_pending) return VBS_ESTATE;
   const int64_t need = static_cast<int64_t>(t_valid) / kv->a.block + 1;
   if (t_valid < 0 || need > kv->a.MB) return VBS_EINVAL;
   if (vbs::bs_can_fuse_remap(a, kv->a)) {
@@ -535,6 +539,7 @@ VBS_EXPORT int bs_step_paged(vbs_bs* c, const void* logits, int64_t ld, float* s
     if (st == VBS_OK) st = vbs::launch_kv_paged_remap(kv->a, beam_idx, t_valid, kv->stream);
   }
   if (st != VBS_OK) return st;
+  kv->copy_pending = true;
   c->step += 1;
   return VBS_OK;
 }
@@ -542,7 +547,9 @@ VBS_EXPORT int bs_step_paged(vbs_bs* c, const void* logits, int64_t ld, float* s
 VBS_EXPORT int kv_paged_copy(vbs_pkv* c) {
   if (!c) return VBS_EINVAL;
   const bool bulk_ok = c->a.slot_bytes % 16 == 0 && aligned16(c->a.pool);
-  return vbs::launch_kv_paged_cow(c->a, bulk_ok, num_sms(), c->stream);
+  const int st = vbs::launch_kv_paged_cow(c->a, bulk_ok, num_sms(), c->stream);
+  if (st == VBS_OK) c->copy_pending = false;
+  return st;
 }
 
 VBS_EXPORT int kv_paged_table(vbs_pkv* c, const int32_t** table, int* max_blocks) {
@@ -571,6 +578,9 @@ VBS_EXPORT int kv_paged_save(vbs_pkv* c) {
 
 VBS_EXPORT int kv_paged_restore(vbs_pkv* c) {
   if (!c) return VBS_EINVAL;
+  // copies still pending refer to the state being dropped: forget them
+  if (cudaMemsetAsync(c->a.tasks, 0, sizeof(int4) * c->R, c->stream) != cudaSuccess) return VBS_ECUDA;
+  c->copy_pending = false;
   return cudaMemcpyAsync(c->state, c->saved, c->state_bytes, cudaMemcpyDeviceToDevice, c->stream) == cudaSuccess
              ? VBS_OK : VBS_ECUDA;
 }

@@ -22,9 +22,8 @@ struct PagedArgs {
   int32_t* refcnt;                // [B*S]
   int32_t* stack;                 // [B*S]
   int32_t* top;                   // [B]
-  int4* tasks;                    // [R] (src block, dst block, filled slots, -)
-  int32_t* task_count;
-  int32_t* cow_ticket;
+  int4* tasks;                    // [R]: sentence b's tasks in [b*W, (b+1)*W) (src block, dst block, filled slots, -)
+  int task_cap;                   // R
   unsigned long long* cow_slots;  // filled slots copied, summed (x L*2*H runs)
   int* status;
 };

@@ -926,7 +926,7 @@ __device__ void cluster_merge_sentence(const BsArgs& a, BsShared& sh, int b, int
   }
 }
 
-template <typename T, bool TMA>
+template <typename T, bool TMA, bool FUSE>
 __global__ void __launch_bounds__(BS_NT, 1) bs_cluster_kernel(const BsArgs a) {
   extern __shared__ __align__(128) unsigned char bs_smem[];
   BsShared& sh = *reinterpret_cast<BsShared*>(bs_smem);
@@ -958,7 +958,7 @@ __global__ void __launch_bounds__(BS_NT, 1) bs_cluster_kernel(const BsArgs a) {
     const int lane = threadIdx.x & 31;
     if (TMA && lane == 0) {
       produce<T>(a, sh, e0, e1);
-    } else if (a.kv_fuse && c == 0) {
+    } else if (FUSE && c == 0) {
       // the idle producer lanes pull the sentence's KV block state into L2 for the
       // remap that follows the merge
       const PagedArgs& kv = a.kv;
@@ -977,7 +977,7 @@ __global__ void __launch_bounds__(BS_NT, 1) bs_cluster_kernel(const BsArgs a) {
   cooperative_groups::this_cluster().sync();       // every CTA's row results are in its shared memory
   if (c == 0 && threadIdx.x < 32) cluster_merge_sentence(a, sh, b, threadIdx.x);
   cooperative_groups::this_cluster().sync();       // keep them readable until the merge is done
-  if (a.kv_fuse && c == 0) {
+  if (FUSE && c == 0) {
     // the paged KV remap of the sentence, on the step's beam_idx just written; the ring is
     // free now and holds its shared state
     RemapShared& rsh = *reinterpret_cast<RemapShared*>(&sh.ring[0][0]);
@@ -1410,12 +1410,12 @@ static int launch_merge(const BsArgs& a, cudaStream_t s) {
   return cudaLaunchKernelEx(&cfg, bs_merge_kernel, a) == cudaSuccess ? VBS_OK : VBS_ECUDA;
 }
 
-template <typename T, bool TMA>
+template <typename T, bool TMA, bool FUSE>
 static int launch_cluster(const BsArgs& a, cudaStream_t s) {
   static bool attr_set = false;
   const int smem = static_cast<int>(sizeof(BsShared));
   if (!attr_set) {
-    if (cudaFuncSetAttribute(bs_cluster_kernel<T, TMA>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+    if (cudaFuncSetAttribute(bs_cluster_kernel<T, TMA, FUSE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
       return VBS_ECUDA;
     attr_set = true;
@@ -1434,13 +1434,19 @@ static int launch_cluster(const BsArgs& a, cudaStream_t s) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, bs_cluster_kernel<T, TMA>, a) == cudaSuccess ? VBS_OK : VBS_ECUDA;
+  return cudaLaunchKernelEx(&cfg, bs_cluster_kernel<T, TMA, FUSE>, a) == cudaSuccess ? VBS_OK : VBS_ECUDA;
 }
 
 int launch_bs_step(const BsArgs& a, int grid, bool vector_ok, cudaStream_t s) {
   if (a.cluster) {
-    if (a.dtype == VBS_BF16) return vector_ok ? launch_cluster<bf16_t, true>(a, s) : launch_cluster<bf16_t, false>(a, s);
-    return vector_ok ? launch_cluster<float, true>(a, s) : launch_cluster<float, false>(a, s);
+    if (a.kv_fuse) {
+      if (a.dtype == VBS_BF16)
+        return vector_ok ? launch_cluster<bf16_t, true, true>(a, s) : launch_cluster<bf16_t, false, true>(a, s);
+      return vector_ok ? launch_cluster<float, true, true>(a, s) : launch_cluster<float, false, true>(a, s);
+    }
+    if (a.dtype == VBS_BF16)
+      return vector_ok ? launch_cluster<bf16_t, true, false>(a, s) : launch_cluster<bf16_t, false, false>(a, s);
+    return vector_ok ? launch_cluster<float, true, false>(a, s) : launch_cluster<float, false, false>(a, s);
   }
   int st;
   if (a.dtype == VBS_BF16)

@@ -209,6 +209,7 @@ int launch_kv_paged_remap(const PagedArgs& a, const int32_t* beam_idx, int t_val
 struct CowMap {
   const char* pool;
   const int4* tasks;
+  int task_cap;
   int n_runs;                       // L * 2 * H
   int64_t block_bytes, run_bytes, slot_bytes;
   __device__ void operator()(int64_t item, const char*& s, char*& d, u32& bytes) const {
@@ -224,7 +225,8 @@ struct CowMap {
 // Copy-on-write items are short (one run's filled slots, a few KB) and scattered, so
 // the copy is warp-per-item with plain 16-byte vectors: each lane issues up to COW_U loads
 // before its stores, and 32 warps per SM keep about 128 KB in flight, which is what HBM
-// latency needs at full bandwidth.  The last CTA to finish clears the task list.
+// latency needs at full bandwidth.  Items cover every row's task slot; a slot the remap
+// left empty (0 filled positions) copies nothing.
 constexpr int COW_NT = 256;
 constexpr int COW_CTAS_PER_SM = 4;
 constexpr int COW_U = 8;
@@ -234,10 +236,10 @@ __device__ __forceinline__ void st_stream16(void* p, const uint4& v) {
                : "memory");
 }
 
-__global__ void __launch_bounds__(COW_NT) kv_cow_vec_kernel(CowMap map, int32_t* task_count, int32_t* cow_ticket) {
+__global__ void __launch_bounds__(COW_NT) kv_cow_vec_kernel(CowMap map) {
   asm volatile("griddepcontrol.wait;" ::: "memory");   // the remap's tasks
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int64_t n_items = static_cast<int64_t>(*task_count) * map.n_runs;
+  const int64_t n_items = static_cast<int64_t>(map.task_cap) * map.n_runs;
   const int lane = threadIdx.x & 31;
   const int64_t nw = static_cast<int64_t>(gridDim.x) * (COW_NT / 32);
   for (int64_t item = static_cast<int64_t>(blockIdx.x) * (COW_NT / 32) + (threadIdx.x >> 5); item < n_items;
@@ -261,20 +263,12 @@ __global__ void __launch_bounds__(COW_NT) kv_cow_vec_kernel(CowMap map, int32_t*
       }
     }
   }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    if (atomicAdd(cow_ticket, 1) == static_cast<int>(gridDim.x) - 1) {
-      *task_count = 0;
-      *cow_ticket = 0;
-    }
-  }
 }
 
-__global__ void kv_cow_plain_kernel(CowMap map, int32_t* task_count, int32_t* cow_ticket) {
+__global__ void kv_cow_plain_kernel(CowMap map) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int64_t n_items = static_cast<int64_t>(*task_count) * map.n_runs;
+  const int64_t n_items = static_cast<int64_t>(map.task_cap) * map.n_runs;
   for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
     const char* s;
     char* d;
@@ -282,25 +276,14 @@ __global__ void kv_cow_plain_kernel(CowMap map, int32_t* task_count, int32_t* co
     map(item, s, d, bytes);
     for (u32 i = threadIdx.x; i < bytes; i += blockDim.x) d[i] = s[i];
   }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    if (atomicAdd(cow_ticket, 1) == static_cast<int>(gridDim.x) - 1) {
-      *task_count = 0;
-      *cow_ticket = 0;
-    }
-  }
 }
 
 int launch_kv_paged_cow(const PagedArgs& a, bool bulk_ok, int num_sms, cudaStream_t s) {
   const int n_runs = a.L * 2 * a.H;
   const int64_t run_bytes = static_cast<int64_t>(a.block) * a.slot_bytes;
-  CowMap m{a.pool, a.tasks, n_runs, a.block_bytes, run_bytes, a.slot_bytes};
-  if (bulk_ok)
-    return launch_pdl(kv_cow_vec_kernel, dim3(num_sms * COW_CTAS_PER_SM), dim3(COW_NT), 0, s, m, a.task_count,
-                      a.cow_ticket);
-  return launch_pdl(kv_cow_plain_kernel, dim3(num_sms * KV_CTAS_PER_SM), dim3(256), 0, s, m, a.task_count,
-                    a.cow_ticket);
+  CowMap m{a.pool, a.tasks, a.task_cap, n_runs, a.block_bytes, run_bytes, a.slot_bytes};
+  if (bulk_ok) return launch_pdl(kv_cow_vec_kernel, dim3(num_sms * COW_CTAS_PER_SM), dim3(COW_NT), 0, s, m);
+  return launch_pdl(kv_cow_plain_kernel, dim3(num_sms * KV_CTAS_PER_SM), dim3(256), 0, s, m);
 }
 
 }  // namespace vbs

@@ -11,7 +11,7 @@
 // between), freed blocks return to the stack in ascending id order, thread 0 makes
 // the block holding position t_valid exclusive to every live row in row order (a
 // fresh block, or a copy-on-write task when it is shared), and the sentence's
-// tasks are reserved with one global atomic.
+// tasks go to its own slots of the task list.
 #pragma once
 
 #include "common.cuh"
@@ -20,9 +20,8 @@
 namespace vbs {
 
 struct RemapShared {
-  int nold[WMAX], par[WMAX], nnew[WMAX], tail[WMAX];
-  int top, any_live, n_tasks;
-  int4 task[WMAX];
+  int nold[WMAX], par[WMAX], nnew[WMAX], tail[WMAX], kept[WMAX];
+  int top;
 };
 
 // Shared-memory ints the remap needs besides RemapShared.
@@ -30,8 +29,10 @@ __host__ __device__ inline int64_t remap_scratch_ints(const PagedArgs& a) {
   return static_cast<int64_t>(a.W) * a.MB + 3 * static_cast<int64_t>(a.S);
 }
 
-// Every thread of the CTA calls it (it synchronises the CTA); bi is the step's
-// beam_idx (global rows, -1 for a finished sentence's pads).
+// Every thread of the CTA calls it (it synchronises the CTA three times); bi is the
+// step's beam_idx (global rows, -1 for a finished sentence's pads).  The sentence's
+// copy-on-write tasks go to its own task slots [b*W, (b+1)*W), unused slots get 0
+// filled positions, so no two sentences contend and the copy kernel needs no count.
 template <int NT>
 __device__ void paged_remap_sentence(const PagedArgs& a, int b, const int32_t* bi, int t_valid, int32_t* rs,
                                      RemapShared& sh) {
@@ -44,10 +45,19 @@ __device__ void paged_remap_sentence(const PagedArgs& a, int b, const int32_t* b
   const int tid = threadIdx.x;
 
   // one round of loads: everything the sentence's remap reads (a finished sentence's
-  // state is read and left as it is)
+  // state is read and left as it is); each of the first W threads checks its row's parent
+  int live = 0;
   if (tid < W) {
     sh.nold[tid] = a.nblk[r0 + tid];
-    sh.par[tid] = __ldcg(bi + r0 + tid);               // the fused caller wrote it in this kernel
+    int p = __ldcg(bi + r0 + tid);                        // a fused caller wrote it in this kernel
+    if (p >= 0) {
+      live = 1;
+      if (p < r0 || p >= r0 + W) {
+        set_status(a.status, VBS_EINVAL);
+        p = -1;
+      }
+    }
+    sh.par[tid] = p;
   }
   for (int i = tid; i < W * MB; i += NT) old[i] = a.table[static_cast<int64_t>(r0) * MB + i];
   for (int j = tid; j < S; j += NT) {
@@ -55,48 +65,31 @@ __device__ void paged_remap_sentence(const PagedArgs& a, int b, const int32_t* b
     rc0[j] = rc[j];
     stk[j] = a.stack[static_cast<int64_t>(b) * S + j];
   }
-  if (tid == 0) {
-    sh.top = a.top[b];
-    sh.n_tasks = 0;
+  if (tid == 0) sh.top = a.top[b];
+  if (!__syncthreads_or(live)) {                          // a finished sentence: nothing moves
+    if (tid < W) a.tasks[r0 + tid] = make_int4(0, 0, 0, 0);
+    return;
   }
-  __syncthreads();
-  if (tid == 0) {
-    int live = 0;
-    for (int w = 0; w < W; ++w) {
-      if (sh.par[w] < 0) continue;
-      live = 1;
-      if (sh.par[w] < r0 || sh.par[w] >= r0 + W) {
-        set_status(a.status, VBS_EINVAL);
-        sh.par[w] = -1;
-      }
-    }
-    sh.any_live = live;
-  }
-  __syncthreads();
-  if (!sh.any_live) return;                            // a finished sentence: nothing moves
 
-  // new references first, then drop the old ones: a block shared by parent and
-  // child never reaches zero in between
+  // reference counts after the step: +1 for every entry a row takes from its parent, -1
+  // for every entry it drops (the final counts do not depend on the order)
   for (int i = tid; i < W * MB; i += NT) {
     const int w = i / MB, s = i - w * MB;
     const int p = sh.par[w];
-    if (p >= 0 && s < sh.nold[p - r0]) {
+    if (p < 0) continue;
+    if (s < sh.nold[p - r0]) {
       const int blk = old[(p - r0) * MB + s] - b * S;
       if (blk >= 0 && blk < S) atomicAdd(&rc[blk], 1);
       else set_status(a.status, VBS_EINVAL);
     }
-  }
-  __syncthreads();
-  for (int i = tid; i < W * MB; i += NT) {
-    const int w = i / MB, s = i - w * MB;
-    if (sh.par[w] >= 0 && s < sh.nold[w]) {
+    if (s < sh.nold[w]) {
       const int blk = old[w * MB + s] - b * S;
       if (blk >= 0 && blk < S) atomicSub(&rc[blk], 1);
     }
   }
   __syncthreads();
-  // freed blocks go back on the stack in ascending id order
   if (tid < 32) {
+    // freed blocks go back on the stack in ascending id order
     for (int j0 = 0; j0 < S; j0 += 32) {
       const int j = j0 + tid;
       const bool freed = j < S && rc0[j] > 0 && rc[j] == 0;
@@ -107,46 +100,40 @@ __device__ void paged_remap_sentence(const PagedArgs& a, int b, const int32_t* b
       if (tid == 0) sh.top = min(S, sh.top + __popc(m));
       __syncwarp();
     }
-  }
-  __syncthreads();
-
-  // make the block holding position t_valid exclusive to each live row
-  if (tid == 0) {
-    const int i = t_valid / a.block, fill = t_valid % a.block;
-    int kept[WMAX];
-    int n_kept = 0;
-    for (int w = 0; w < W; ++w) {
-      sh.tail[w] = -1;
-      const int p = sh.par[w];
-      if (p < 0) { sh.nnew[w] = sh.nold[w]; continue; }
-      const int n = sh.nold[p - r0];
-      sh.nnew[w] = n;
-      if (n == i) {                                       // a fresh block, nothing to copy
-        if (sh.top == 0) { set_status(a.status, VBS_ENOMEM); continue; }
-        const int nb = stk[--sh.top];
-        rc[nb - b * S] = 1;
-        sh.tail[w] = nb;
-        sh.nnew[w] = i + 1;
-      } else if (n == i + 1) {
-        const int blk = old[(p - r0) * MB + i];
-        if (rc[blk - b * S] == 1) continue;
-        bool is_kept = false;
-        for (int q = 0; q < n_kept; ++q) is_kept |= kept[q] == blk;
-        if (!is_kept) { kept[n_kept++] = blk; continue; }  // the lowest row keeps the shared block
-        if (sh.top == 0) { set_status(a.status, VBS_ENOMEM); continue; }
-        const int nb = stk[--sh.top];
-        rc[nb - b * S] = 1;
-        rc[blk - b * S] -= 1;
-        sh.tail[w] = nb;
-        sh.task[sh.n_tasks++] = make_int4(blk, nb, fill, 0);
-      } else {
-        set_status(a.status, VBS_EINVAL);                 // the table does not match t_valid
+    // make the block holding position t_valid exclusive to each live row, in row order
+    if (tid == 0) {
+      const int i = t_valid / a.block, fill = t_valid % a.block;
+      int n_kept = 0, n_tasks = 0;
+      for (int w = 0; w < W; ++w) {
+        sh.tail[w] = -1;
+        const int p = sh.par[w];
+        if (p < 0) { sh.nnew[w] = sh.nold[w]; continue; }
+        const int n = sh.nold[p - r0];
+        sh.nnew[w] = n;
+        if (n == i) {                                     // a fresh block, nothing to copy
+          if (sh.top == 0) { set_status(a.status, VBS_ENOMEM); continue; }
+          const int nb = stk[--sh.top];
+          rc[nb - b * S] = 1;
+          sh.tail[w] = nb;
+          sh.nnew[w] = i + 1;
+        } else if (n == i + 1) {
+          const int blk = old[(p - r0) * MB + i];
+          if (rc[blk - b * S] == 1) continue;
+          bool is_kept = false;
+          for (int q = 0; q < n_kept; ++q) is_kept |= sh.kept[q] == blk;
+          if (!is_kept) { sh.kept[n_kept++] = blk; continue; }   // the lowest row keeps the shared block
+          if (sh.top == 0) { set_status(a.status, VBS_ENOMEM); continue; }
+          const int nb = stk[--sh.top];
+          rc[nb - b * S] = 1;
+          rc[blk - b * S] -= 1;
+          sh.tail[w] = nb;
+          a.tasks[r0 + n_tasks++] = make_int4(blk, nb, fill, 0);
+        } else {
+          set_status(a.status, VBS_EINVAL);               // the table does not match t_valid
+        }
       }
-    }
-    if (sh.n_tasks) {                                     // one reservation for the sentence's copies
-      const int base = atomicAdd(a.task_count, sh.n_tasks);
-      for (int q = 0; q < sh.n_tasks; ++q) a.tasks[base + q] = sh.task[q];
-      atomicAdd(a.cow_slots, static_cast<unsigned long long>(sh.n_tasks) * fill * (a.L * 2 * a.H));
+      for (int q = n_tasks; q < W; ++q) a.tasks[r0 + q] = make_int4(0, 0, 0, 0);
+      if (n_tasks) atomicAdd(a.cow_slots, static_cast<unsigned long long>(n_tasks) * fill * (a.L * 2 * a.H));
     }
   }
   __syncthreads();
