@@ -233,6 +233,10 @@ __device__ __forceinline__ void st_release_u64(u64* p, u64 v) {
   asm volatile("st.release.gpu.global.u64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
 }
 
+__device__ __forceinline__ void prefetch_row_l2(const char* p, int64_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p), "r"(static_cast<unsigned>(bytes)) : "memory");
+}
+
 template <typename T, bool VECTOR>
 __global__ void __launch_bounds__(BPD_RT, 3) bpd_verify_queue_kernel(const void* logits, const int32_t* proposals, int B,
                                                                   int k, int V, int eos, int32_t* khat_out,
@@ -266,6 +270,9 @@ __global__ void __launch_bounds__(BPD_RT, 3) bpd_verify_queue_kernel(const void*
         if (__ldg(props + e) == eos) { checks = min(checks, e); break; }
     int n = 1, am = -1;
     for (int p = 0; p < checks; ++p) {
+      // the next head-0 row is read unless this check fails: start it towards L2
+      if (VECTOR && tid == 0 && p + 1 <= checks)
+        prefetch_row_l2(base + static_cast<int64_t>(p + 1) * k * row_bytes, row_bytes);
       am = row_argmax<T, VECTOR>(base + static_cast<int64_t>(p) * k * row_bytes, V, st, red, status);
       if (__ldg(props + p + 1) != am) break;
       ++n;
