@@ -24,6 +24,19 @@ B1 (layout) ``logits[b, p, h, :]`` holds head h+1 (p_{h+1}) at proposal position
 B2 (ties) argmax breaks ties toward the lower token id.
 B3 (EOS) greedy stops at EOS (§2); if an accepted proposal e < khat is EOS,
    khat becomes e + 1.
+
+§5 approximate inference relaxes the verify test; the criteria's formulas are
+missing from the pages' text, so these are the readings (exact when the
+parameters are 1, 0, 1):
+A1 (top-k, §5.1) proposal p+1 passes when it is among the ``param`` best tokens
+   of head 0 at position p: its rank, the number of tokens with a larger logit
+   or an equal logit and a lower id (B2), is below ``param`` (>= 1).
+A2 (distance, §5.2) with d(u, v) = |u - v| on token ids read as intensities,
+   proposal p+1 passes when |proposal - argmax| <= ``param`` (>= 0).
+A3 (minimum block, §5.3) at least ``min_accept`` (1..k) tokens are accepted:
+   khat = max(khat, min_accept), and the EOS cut (B3) applies after it.
+   min_accept = k decodes in fixed blocks of k.  The next proposals come from
+   position khat - 1 as always.
 """
 
 from __future__ import annotations
@@ -34,6 +47,27 @@ import numpy as np
 def argmax_first(row) -> int:
     """argmax with ties to the lowest index (numpy returns the first occurrence)."""
     return int(np.argmax(np.asarray(row, dtype=np.float64)))
+
+
+EXACT, TOPK, DISTANCE = 0, 1, 2
+
+
+def rank_of(row, tok: int) -> int:
+    """How many tokens beat ``tok``: a larger logit, or an equal one at a lower id (B2)."""
+    x = np.asarray(row, dtype=np.float64)
+    xt = x[tok]
+    return int(np.count_nonzero(x > xt) + np.count_nonzero(x[:tok] == xt))
+
+
+def passes(row, proposal: int, criterion: int = EXACT, param: int = 0) -> bool:
+    """The verify test of one proposal against head 0's row (§3, or A1 / A2)."""
+    if criterion == EXACT:
+        return proposal == argmax_first(row)
+    if criterion == TOPK:
+        return 0 <= proposal < len(row) and rank_of(row, proposal) < param
+    if criterion == DISTANCE:
+        return abs(proposal - argmax_first(row)) <= param
+    raise ValueError(f"unknown criterion {criterion}")
 
 
 def propose(logits) -> np.ndarray:
@@ -47,8 +81,9 @@ def propose(logits) -> np.ndarray:
     return out
 
 
-def verify(logits, proposals, eos: int = -1):
-    """Verify + accept on combined-model logits [B, k, k, V] (B1-B3).
+def verify(logits, proposals, eos: int = -1, criterion: int = EXACT, param: int = 0, min_accept: int = 1):
+    """Verify + accept on combined-model logits [B, k, k, V] (B1-B3; A1-A3 for the
+    approximate criteria).
 
     Returns (khat [B], next_proposals [B, k]).
     """
@@ -60,10 +95,11 @@ def verify(logits, proposals, eos: int = -1):
     for b in range(B):
         n = 1
         for p in range(k - 1):
-            if int(props[b, p + 1]) == argmax_first(x[b, p, 0]):
+            if passes(x[b, p, 0], int(props[b, p + 1]), criterion, param):
                 n += 1
             else:
                 break
+        n = max(n, min(min_accept, k))
         if eos >= 0:
             for e in range(n):
                 if int(props[b, e]) == eos:

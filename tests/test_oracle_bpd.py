@@ -93,3 +93,95 @@ def test_verify_eos_truncates_and_khat_bounds():
     assert list(kh) == [3, 3]                                   # accepted up to and incl. EOS
     kh, _ = ob.verify(logits, props, eos=1)
     assert list(kh) == [1, 1]
+
+
+# --- §5 approximate criteria (readings A1-A3) ---------------------------------------
+
+def _hand_rows():
+    """One element, k = 3, V = 6.  Head 0 at position 0 ranks the tokens 1, 2, 3, 5, 0, 4
+    (tokens 2 and 3 tie at 2.0: the lower id ranks first); head 0 at position 1 has argmax 4.
+    Heads 1 and 2 have argmax 0 and 1 everywhere."""
+    x = np.full((1, 3, 3, 6), -2.0)
+    x[0, :, 1, 0] = 5.0
+    x[0, :, 2, 1] = 5.0
+    x[0, 0, 0] = [0.1, 3.0, 2.0, 2.0, -1.0, 0.5]
+    x[0, 1, 0] = [0.0, 0.0, 0.0, 0.0, 1.0, 0.0]
+    x[0, 2, 0] = [0.0, 0.0, 0.0, 0.0, 0.0, 1.0]
+    return x
+
+
+def test_rank_counts_larger_and_lower_equal_tokens():
+    row = [0.1, 3.0, 2.0, 2.0, -1.0, 0.5]
+    assert [ob.rank_of(row, t) for t in range(6)] == [4, 0, 1, 2, 5, 3]
+
+
+def test_topk_accepts_a_proposal_by_its_rank():
+    x = _hand_rows()
+    props = np.array([[0, 3, 4]])            # token 3 has rank 2 at position 0; 4 is the argmax at 1
+    assert ob.verify(x, props)[0][0] == 1
+    assert ob.verify(x, props, criterion=ob.TOPK, param=1)[0][0] == 1
+    assert ob.verify(x, props, criterion=ob.TOPK, param=2)[0][0] == 1
+    kh, nxt = ob.verify(x, props, criterion=ob.TOPK, param=3)
+    assert kh[0] == 3 and list(nxt[0]) == [5, 0, 1]   # next proposals from position 2
+    props2 = np.array([[0, 2, 4]])           # token 2 ties token 3 but has the lower id: rank 1
+    assert ob.verify(x, props2, criterion=ob.TOPK, param=2)[0][0] == 3
+
+
+def test_distance_accepts_a_near_token():
+    x = _hand_rows()
+    props = np.array([[0, 2, 5]])            # |2 - 1| = 1 at position 0, |5 - 4| = 1 at position 1
+    assert ob.verify(x, props, criterion=ob.DISTANCE, param=0)[0][0] == 1
+    assert ob.verify(x, props, criterion=ob.DISTANCE, param=1)[0][0] == 3
+    props = np.array([[0, 3, 4]])            # |3 - 1| = 2
+    assert ob.verify(x, props, criterion=ob.DISTANCE, param=1)[0][0] == 1
+    assert ob.verify(x, props, criterion=ob.DISTANCE, param=2)[0][0] == 3
+
+
+def test_minimum_block_and_its_eos_cut():
+    x = _hand_rows()
+    props = np.array([[0, 5, 5]])            # fails at position 0
+    kh, nxt = ob.verify(x, props, min_accept=2)
+    assert kh[0] == 2 and list(nxt[0]) == [4, 0, 1]  # next proposals from position 1
+    assert ob.verify(x, props, min_accept=3)[0][0] == 3
+    assert ob.verify(x, props, min_accept=3, eos=5)[0][0] == 2   # proposal 1 is EOS: stop after it
+    assert ob.verify(x, props, min_accept=9)[0][0] == 3          # at most k
+
+
+def _random_case(seed, B=24, k=5, V=11):
+    rng = np.random.default_rng(seed)
+    x = np.round(rng.normal(size=(B, k, k, V)) * 2) / 2   # half-integers: ties happen
+    g = x[:, :, 0].argmax(-1)
+    props = rng.integers(0, V, size=(B, k))
+    agree = rng.random((B, k)) < 0.6
+    props[:, 1:] = np.where(agree[:, 1:], g[:, :-1], props[:, 1:])
+    return x, props
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_relaxed_criteria_reduce_to_exact(seed):
+    x, props = _random_case(seed)
+    kh, nx = ob.verify(x, props, eos=3)
+    for crit, param in ((ob.TOPK, 1), (ob.DISTANCE, 0)):
+        kh2, nx2 = ob.verify(x, props, eos=3, criterion=crit, param=param, min_accept=1)
+        np.testing.assert_array_equal(kh2, kh)
+        np.testing.assert_array_equal(nx2, nx)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_khat_grows_with_the_relaxation(seed):
+    x, props = _random_case(seed)
+    B, k, _, V = x.shape
+    prev = ob.verify(x, props, criterion=ob.TOPK, param=1)[0]
+    for param in range(2, V + 1):
+        kh = ob.verify(x, props, criterion=ob.TOPK, param=param)[0]
+        assert (kh >= prev).all()
+        prev = kh
+    assert (prev == k).all()                 # every token is in the top V
+    prev = ob.verify(x, props, criterion=ob.DISTANCE, param=0)[0]
+    for param in range(1, V):
+        kh = ob.verify(x, props, criterion=ob.DISTANCE, param=param)[0]
+        assert (kh >= prev).all()
+        prev = kh
+    assert (prev == k).all()
+    for m in range(1, k + 1):
+        assert (ob.verify(x, props, min_accept=m)[0] >= m).all()
