@@ -310,6 +310,11 @@ int vbs_stateless_status(vbs_stream_t stream);
  * Blockwise parallel decoding ([BPD] §3-§4)
  * ============================================================================= */
 
+/* The verify test of bpd_verify_approx ([BPD] §3 exact, §5.1 top-k, §5.2 distance). */
+#define VBS_BPD_EXACT 0
+#define VBS_BPD_TOPK 1
+#define VBS_BPD_DISTANCE 2
+
 /*
  * Predict: proposals[b, h] = argmax_v logits[b, h, v] for logits [B, k, V]
  * (device, dense rows); argmax ties go to the lower token id.
@@ -332,6 +337,23 @@ int bpd_propose(const void* logits, int B, int k, int V, int dtype, int32_t* pro
  */
 int bpd_verify(const void* logits, const int32_t* proposals, int B, int k, int V, int dtype, int eos,
                int32_t* khat, int32_t* next, vbs_stream_t stream);
+/*
+ * bpd_verify with the relaxed verify tests of [BPD] §5 (approximate inference:
+ * the output may differ from greedy decoding).  The pages' formulas for the
+ * criteria are missing from their text; these are the readings:
+ *   criterion VBS_BPD_EXACT: proposal == argmax (bpd_verify; param ignored);
+ *   VBS_BPD_TOPK (§5.1): the proposal's rank in head 0's row -- the number of
+ *     tokens with a larger logit, or an equal logit and a lower id -- is below
+ *     param (param >= 1; 1 is exact);
+ *   VBS_BPD_DISTANCE (§5.2): |proposal - argmax| <= param, token ids read as
+ *     intensities with d(u, v) = |u - v| (param >= 0; 0 is exact).
+ * min_accept (§5.3, 1..k): khat = max(khat, min_accept) before the EOS cut;
+ * min_accept = k decodes in fixed blocks of k.  The next proposals come from
+ * position khat-1 as in bpd_verify.  Same layout, ownership and queue notes.
+ * Errors: VBS_EINVAL for an unknown criterion or a parameter out of range.
+ */
+int bpd_verify_approx(const void* logits, const int32_t* proposals, int B, int k, int V, int dtype, int eos,
+                      int criterion, int param, int min_accept, int32_t* khat, int32_t* next, vbs_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -182,6 +182,43 @@ def planted_rows(argmax_tokens: torch.Tensor, V: int, *, seed: int, salt: int,
     return x.to(dtype).reshape(*shape, V) if argmax_tokens.numel() else x[:0].to(dtype).reshape(*shape, V)
 
 
+def near_miss_proposals(B: int, k: int, V: int, *, seed: int, step: int, sigma: float = 2.0,
+                        dtype=torch.bfloat16, device="cpu"):
+    """Verify-step inputs where proposals often miss the base model's argmax narrowly.
+
+    Every row of logits [B, k, k, V] is N(0, sigma) noise; head 0's rows get three
+    planted tokens above the noise (first, second and third, spaced by a third of a
+    U(0.5, 2) lift), the other heads one planted argmax.  Proposal q >= 1 is, by a
+    coin, head 0's first (40 %), second (15 %) or third (10 %) token at position q-1,
+    its first token +-1 or +-2 (15 %, clipped to [0, V)), or uniform (20 %).
+    Returns (logits, proposals int64 [B, k]).
+    """
+    g_ = _gen(mix_seed(seed, 0xD1, step), "cpu")
+    x = torch.randn(B, k, k, V, generator=g_) * sigma
+    lift = 0.5 + 1.5 * torch.rand(B, k, k, generator=g_)
+    top = x.max(dim=-1).values + lift
+    tok = torch.stack([torch.randperm(V, generator=g_)[:3] for _ in range(B * k * k)]).reshape(B, k, k, 3)
+    for r in range(3):
+        val = top - lift * (r / 3.0)
+        keep = torch.ones(B, k, k, dtype=torch.bool) if r == 0 else torch.zeros(B, k, k, dtype=torch.bool)
+        keep[:, :, 0] = True
+        cur = x.gather(-1, tok[..., r:r + 1]).squeeze(-1)
+        x.scatter_(-1, tok[..., r:r + 1], torch.where(keep, val, cur).unsqueeze(-1))
+    props = torch.randint(0, V, (B, k), generator=g_)
+    coin = torch.rand(B, k, generator=g_)
+    shift = torch.tensor([-2, -1, 1, 2])[torch.randint(0, 4, (B, k), generator=g_)]
+    first = tok[:, :, 0, 0]
+    for q in range(1, k):
+        c = coin[:, q]
+        near = (first[:, q - 1] + shift[:, q]).clamp(0, V - 1)
+        pick = torch.where(c < 0.40, first[:, q - 1],
+               torch.where(c < 0.55, tok[:, q - 1, 0, 1],
+               torch.where(c < 0.65, tok[:, q - 1, 0, 2],
+               torch.where(c < 0.80, near, props[:, q]))))
+        props[:, q] = pick
+    return x.to(dtype).to(device), props.to(device)
+
+
 def geometric_prefix_proposals(B: int, k: int, V: int, *, seed: int, step: int, p: float = 0.7,
                                device="cpu"):
     """Verify-step inputs with a planted agreement structure.

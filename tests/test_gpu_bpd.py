@@ -153,3 +153,68 @@ def test_verify_on_both_sides_of_the_queue_limit(B, k):
     np.testing.assert_array_equal(khat.cpu().numpy()[pick], ekh)
     np.testing.assert_array_equal(nxt.cpu().numpy()[pick], enx)
     assert vbs.lib().vbs_stateless_status(vbs._stream()) == 0
+
+
+# --- the relaxed verify tests of §5 (bpd_verify_approx) --------------------------------
+
+_CRITERIA = [(0, 0, 1), (1, 2, 1), (1, 3, 1), (1, 1, 1), (2, 1, 1), (2, 2, 1), (2, 0, 1), (0, 0, 3), (1, 2, 4),
+             (2, 1, 5)]
+
+
+@pytest.mark.parametrize("B,k,V,dtype,eos", [
+    (40, 5, 1000, torch.bfloat16, -1),
+    (33, 6, 4096, torch.float32, 7),
+    (17, 8, 32000, torch.bfloat16, -1),
+    (13, 4, 77, torch.bfloat16, -1),        # element path
+    (9, 3, 3001, torch.float32, 11),        # element path (V * 4 not a multiple of 16), EOS
+])
+def test_relaxed_verify_matches_oracle(B, k, V, dtype, eos):
+    import verify_bs_step_gb300 as vbs
+    logits, props = synth.near_miss_proposals(B, k, V, seed=B * 7 + k, step=V % 13, dtype=dtype)
+    if eos >= 0:
+        props[1::3, min(2, k - 1)] = eos
+    lg, pr = logits.cuda(), props.to(torch.int32).cuda()
+    x = _np(logits)
+    for crit, param, ma in _CRITERIA:
+        ma = min(ma, k)
+        khat, nxt = vbs.bpd_verify(lg, pr, eos, criterion=crit, param=param, min_accept=ma)
+        ekh, enx = ob.verify(x, props.numpy(), eos, crit, param, ma)
+        np.testing.assert_array_equal(khat.cpu().numpy(), ekh, err_msg=f"khat {crit} {param} {ma}")
+        np.testing.assert_array_equal(nxt.cpu().numpy(), enx, err_msg=f"next {crit} {param} {ma}")
+    assert vbs.lib().vbs_stateless_status(vbs._stream()) == 0
+
+
+def test_relaxed_verify_out_of_range_proposal_fails_topk():
+    import verify_bs_step_gb300 as vbs
+    B, k, V = 4, 3, 64
+    logits, props = synth.near_miss_proposals(B, k, V, seed=2, step=0, dtype=torch.float32)
+    props[:, 1] = torch.tensor([V, -1, V + 5, 0])
+    khat, nxt = vbs.bpd_verify(logits.cuda(), props.to(torch.int32).cuda(), -1, criterion=vbs.BPD_TOPK, param=V)
+    ekh, enx = ob.verify(_np(logits), props.numpy(), -1, ob.TOPK, V, 1)
+    np.testing.assert_array_equal(khat.cpu().numpy(), ekh)
+    np.testing.assert_array_equal(nxt.cpu().numpy(), enx)
+
+
+@pytest.mark.parametrize("B", [16384, 16385])
+def test_relaxed_verify_on_both_sides_of_the_queue_limit(B):
+    import verify_bs_step_gb300 as vbs
+    k, V = 3, 64
+    logits, props = synth.near_miss_proposals(B, k, V, seed=B, step=1, dtype=torch.bfloat16)
+    lg, pr = logits.cuda(), props.to(torch.int32).cuda()
+    pick = np.r_[0:64, B - 64:B]
+    x = _np(logits[pick])
+    for crit, param, ma in ((1, 2, 1), (2, 1, 2)):
+        khat, nxt = vbs.bpd_verify(lg, pr, -1, criterion=crit, param=param, min_accept=ma)
+        ekh, enx = ob.verify(x, props[pick].numpy(), -1, crit, param, ma)
+        np.testing.assert_array_equal(khat.cpu().numpy()[pick], ekh)
+        np.testing.assert_array_equal(nxt.cpu().numpy()[pick], enx)
+
+
+def test_relaxed_verify_rejects_bad_parameters():
+    import verify_bs_step_gb300 as vbs
+    logits, props = synth.near_miss_proposals(2, 3, 64, seed=1, step=0, dtype=torch.float32)
+    lg, pr = logits.cuda(), props.to(torch.int32).cuda()
+    for crit, param, ma in ((1, 0, 1), (2, -1, 1), (3, 0, 1), (0, 0, 0), (0, 0, 4)):
+        with pytest.raises(vbs.VbsError) as e:
+            vbs.bpd_verify(lg, pr, -1, criterion=crit, param=param, min_accept=ma)
+        assert e.value.status == vbs.EINVAL

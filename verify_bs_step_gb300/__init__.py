@@ -14,10 +14,12 @@ import os
 import torch
 
 __all__ = ["BeamSearch", "PagedKV", "kv_reorder", "bpd_propose", "bpd_verify", "VbsError", "lib",
-           "LP_GNMT", "LP_POWER", "ES_FALSE", "ES_TRUE", "ES_NEVER", "F32", "BF16"]
+           "LP_GNMT", "LP_POWER", "ES_FALSE", "ES_TRUE", "ES_NEVER", "F32", "BF16", "BPD_EXACT", "BPD_TOPK",
+           "BPD_DISTANCE"]
 
 F32, BF16 = 0, 1
 LP_GNMT, LP_POWER = 0, 1
+BPD_EXACT, BPD_TOPK, BPD_DISTANCE = 0, 1, 2
 ES_FALSE, ES_TRUE, ES_NEVER = 0, 1, 2
 OK, EINVAL, ECUDA, ENOMEM, ESTATE, EALIGN, ETIMEOUT, EINPUT, ESCRATCH = 0, -1, -2, -3, -4, -5, -6, -7, -8
 
@@ -59,6 +61,8 @@ SIGNATURES = {
     "kv_paged_destroy": (_c_int, [_vp]),
     "bpd_propose": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _vp, _vp]),
     "bpd_verify": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _vp]),
+    "bpd_verify_approx": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp,
+                                   _vp]),
 }
 
 _LIB = None
@@ -356,8 +360,12 @@ def bpd_propose(logits: torch.Tensor, out: torch.Tensor | None = None) -> torch.
 
 
 def bpd_verify(logits: torch.Tensor, proposals: torch.Tensor, eos: int = -1, khat: torch.Tensor | None = None,
-               next_out: torch.Tensor | None = None):
-    """Verify + accept on combined logits [B, k, k, V] -> (khat int32 [B], next proposals int32 [B, k])."""
+               next_out: torch.Tensor | None = None, criterion: int = 0, param: int = 0, min_accept: int = 1):
+    """Verify + accept on combined logits [B, k, k, V] -> (khat int32 [B], next proposals int32 [B, k]).
+
+    criterion BPD_EXACT (default), BPD_TOPK (param = top-k size) or BPD_DISTANCE (param =
+    largest token distance), and min_accept (the minimum accepted block): the relaxed
+    verify of bpd_verify_approx."""
     if logits.dim() != 4 or logits.shape[1] != logits.shape[2] or not logits.is_contiguous():
         raise ValueError("logits must be a contiguous [B, k, k, V] tensor")
     B, k, _, V = logits.shape
@@ -367,7 +375,13 @@ def bpd_verify(logits: torch.Tensor, proposals: torch.Tensor, eos: int = -1, kha
         khat = torch.empty(B, dtype=torch.int32, device=logits.device)
     if next_out is None:
         next_out = torch.empty(B, k, dtype=torch.int32, device=logits.device)
-    _check(lib().bpd_verify(_dev_ptr(logits, "logits"), _dev_ptr(proposals, "proposals", torch.int32), B, k, V,
-                            _dtype_code(logits.dtype), eos, _dev_ptr(khat, "khat", torch.int32),
-                            _dev_ptr(next_out, "next", torch.int32), _stream(logits.device)), "bpd_verify")
+    if criterion == BPD_EXACT and min_accept == 1:
+        _check(lib().bpd_verify(_dev_ptr(logits, "logits"), _dev_ptr(proposals, "proposals", torch.int32), B, k, V,
+                                _dtype_code(logits.dtype), eos, _dev_ptr(khat, "khat", torch.int32),
+                                _dev_ptr(next_out, "next", torch.int32), _stream(logits.device)), "bpd_verify")
+    else:
+        _check(lib().bpd_verify_approx(_dev_ptr(logits, "logits"), _dev_ptr(proposals, "proposals", torch.int32), B,
+                                       k, V, _dtype_code(logits.dtype), eos, criterion, param, min_accept,
+                                       _dev_ptr(khat, "khat", torch.int32), _dev_ptr(next_out, "next", torch.int32),
+                                       _stream(logits.device)), "bpd_verify_approx")
     return khat, next_out

@@ -631,15 +631,27 @@ VBS_EXPORT int bpd_propose(const void* logits, int B, int k, int V, int dtype, i
   return vbs::launch_bpd_propose(logits, B, k, V, dtype, vec_ok, proposals, reinterpret_cast<cudaStream_t>(stream));
 }
 
-VBS_EXPORT int bpd_verify(const void* logits, const int32_t* proposals, int B, int k, int V, int dtype, int eos,
-                          int32_t* khat, int32_t* next, vbs_stream_t stream) {
+VBS_EXPORT int bpd_verify_approx(const void* logits, const int32_t* proposals, int B, int k, int V, int dtype,
+                                 int eos, int criterion, int param, int min_accept, int32_t* khat, int32_t* next,
+                                 vbs_stream_t stream) {
   if (B < 0 || k < 1 || k > vbs::KMAX || V < 1 || (dtype != VBS_F32 && dtype != VBS_BF16)) return VBS_EINVAL;
   if (B > 0 && (!logits || !proposals || !khat || !next)) return VBS_EINVAL;
   if (eos >= V) return VBS_EINVAL;
+  if (criterion == VBS_BPD_EXACT) param = 0;
+  else if (criterion == VBS_BPD_TOPK) { if (param < 1) return VBS_EINVAL; }
+  else if (criterion == VBS_BPD_DISTANCE) { if (param < 0) return VBS_EINVAL; }
+  else return VBS_EINVAL;
+  if (min_accept < 1 || min_accept > k) return VBS_EINVAL;
   const int es = dtype == VBS_BF16 ? 2 : 4;
   const bool vec_ok = aligned16(logits) && (static_cast<int64_t>(V) * es) % 16 == 0;
   int* status = nullptr;
   if (cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_stateless_status) != cudaSuccess) return VBS_ECUDA;
-  return vbs::launch_bpd_verify(logits, proposals, B, k, V, dtype, vec_ok, eos, khat, next, status, num_sms(),
+  const vbs::BpdCrit crit{criterion, param, min_accept};
+  return vbs::launch_bpd_verify(logits, proposals, B, k, V, dtype, vec_ok, eos, crit, khat, next, status, num_sms(),
                                 reinterpret_cast<cudaStream_t>(stream));
+}
+
+VBS_EXPORT int bpd_verify(const void* logits, const int32_t* proposals, int B, int k, int V, int dtype, int eos,
+                          int32_t* khat, int32_t* next, vbs_stream_t stream) {
+  return bpd_verify_approx(logits, proposals, B, k, V, dtype, eos, VBS_BPD_EXACT, 0, 1, khat, next, stream);
 }

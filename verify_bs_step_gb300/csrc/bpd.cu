@@ -23,11 +23,30 @@ constexpr int BPD_NT = 512;
 constexpr int BPD_NW = BPD_NT / 32;
 constexpr int BPD_U = 8;
 
-// Best key of the vectors [i0, i1) of one row, for this thread (strided by `stride`).
-template <typename T, bool VECTOR>
-__device__ __forceinline__ u64 thread_row_best(const char* row, int64_t i0, int64_t i1, int64_t stride) {
+// The verify test of one proposal (§3, or the relaxed tests of §5): exact match with
+// the argmax; rank (keys above the proposal's, ties to the lower id) below crit.param;
+// or a token distance |proposal - argmax| of at most crit.param.
+__device__ __forceinline__ bool bpd_passes(const BpdCrit& crit, int prop, int am, int rank, int V) {
+  if (crit.mode == VBS_BPD_TOPK) return prop >= 0 && prop < V && rank < crit.param;
+  if (crit.mode == VBS_BPD_DISTANCE) return abs(prop - am) <= crit.param;
+  return prop == am;
+}
+
+// The key of token `tok` in a row (0 for a token outside [0, V), which passes no rank test).
+template <typename T>
+__device__ __forceinline__ u64 token_key(const char* row, int tok, int V) {
+  if (tok < 0 || tok >= V) return 0ull;
+  return make_key(Elem<T>::load(row, tok), static_cast<u32>(tok));
+}
+
+// Best key of the vectors [i0, i1) of one row, for this thread (strided by `stride`);
+// with RANK, *cnt also counts this thread's keys above `ref`.
+template <typename T, bool VECTOR, bool RANK = false>
+__device__ __forceinline__ u64 thread_row_best(const char* row, int64_t i0, int64_t i1, int64_t stride,
+                                               u64 ref = 0, int* cnt = nullptr) {
   constexpr int VEC = VECTOR ? Vec16<T>::N : 1;
   u64 best = 0;
+  int c = 0;
   for (int64_t base = i0; base < i1; base += stride * BPD_U) {
     uint4 q[BPD_U];
     float xs[BPD_U];
@@ -50,36 +69,52 @@ __device__ __forceinline__ u64 thread_row_best(const char* row, int64_t i0, int6
         for (int e = 0; e < VEC; ++e) {
           u64 k = make_key(x[e], static_cast<u32>(i * VEC + e));
           best = k > best ? k : best;
+          if constexpr (RANK) c += k > ref ? 1 : 0;
         }
       }
     }
   }
+  if constexpr (RANK) *cnt = c;
   return best;
 }
 
-template <typename T, bool VECTOR>
-__device__ __forceinline__ int cta_row_argmax(const char* row, int64_t nvec, u64* red) {
+// The row's argmax; with RANK also *rank = the number of keys above `ref` (every thread).
+template <typename T, bool VECTOR, bool RANK = false>
+__device__ __forceinline__ int cta_row_argmax(const char* row, int64_t nvec, u64* red, int* redc, u64 ref = 0,
+                                              int* rank = nullptr) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  u64 k = thread_row_best<T, VECTOR>(row, tid, nvec, BPD_NT);
+  int c = 0;
+  u64 k = thread_row_best<T, VECTOR, RANK>(row, tid, nvec, BPD_NT, ref, &c);
   k = warp_max_u64(k);
-  if (lane == 0) red[warp] = k;
+  if constexpr (RANK) c = __reduce_add_sync(FULL, c);
+  if (lane == 0) {
+    red[warp] = k;
+    if constexpr (RANK) redc[warp] = c;
+  }
   __syncthreads();
   if (warp == 0) {
     u64 v = lane < BPD_NW ? red[lane] : 0ull;
     v = warp_max_u64(v);
+    if constexpr (RANK) {
+      const int cc = __reduce_add_sync(FULL, lane < BPD_NW ? redc[lane] : 0);
+      if (lane == 0) redc[BPD_NW] = cc;
+    }
     if (lane == 0) red[BPD_NW] = v;
   }
   __syncthreads();
   const int am = static_cast<int>(key_v(red[BPD_NW]));
+  if constexpr (RANK) *rank = redc[BPD_NW];
   __syncthreads();
   return am;
 }
 
-template <typename T, bool VECTOR>
+template <typename T, bool VECTOR, bool RANK>
 __global__ void __launch_bounds__(BPD_NT) bpd_verify_kernel(const void* logits, const int32_t* proposals, int k,
-                                                           int V, int eos, int32_t* khat_out, int32_t* next_out) {
+                                                           int V, int eos, BpdCrit crit, int32_t* khat_out,
+                                                           int32_t* next_out) {
   constexpr int VEC = VECTOR ? Vec16<T>::N : 1;
   __shared__ u64 red[BPD_NW + 1];
+  __shared__ int redc[BPD_NW + 1];
   __shared__ u64 part[KMAX];
   __shared__ int am_p[KMAX];
   const int b = blockIdx.x;
@@ -90,15 +125,19 @@ __global__ void __launch_bounds__(BPD_NT) bpd_verify_kernel(const void* logits, 
   auto row_ptr = [&](int p, int h) { return base + (static_cast<int64_t>(p) * k + h) * row_bytes; };
   const int32_t* props = proposals + static_cast<int64_t>(b) * k;
 
-  // verify: head 0 at position p must reproduce proposal p+1
+  // verify: head 0 at position p must pass proposal p+1
   int n = 1, last_p = -1;
   for (int p = 0; p < k - 1; ++p) {
-    const int am = cta_row_argmax<T, VECTOR>(row_ptr(p, 0), nvec, red);
+    const int prop = __ldg(props + p + 1);
+    int rank = 0;
+    const u64 ref = RANK ? token_key<T>(row_ptr(p, 0), prop, V) : 0ull;
+    const int am = cta_row_argmax<T, VECTOR, RANK>(row_ptr(p, 0), nvec, red, redc, ref, &rank);
     if (tid == 0) am_p[p] = am;
     last_p = p;
-    if (__ldg(props + p + 1) != am) break;
+    if (!bpd_passes(crit, prop, am, rank, V)) break;
     ++n;
   }
+  n = max(n, min(crit.min_accept, k));                 // the minimum block (§5.3), then the EOS cut
   if (eos >= 0) {
     for (int e = 0; e < n; ++e)
       if (__ldg(props + e) == eos) { n = e + 1; break; }
@@ -145,11 +184,14 @@ struct RowStage {
   u32 phase;
 };
 
-template <typename T, bool VECTOR>
-__device__ int row_argmax(const char* row, int V, RowStage& st, u64* red, int* status) {
+// The row's argmax; with RANK also *rank = the number of keys above `ref`.
+template <typename T, bool VECTOR, bool RANK = false>
+__device__ int row_argmax(const char* row, int V, RowStage& st, u64* red, int* status, int* redc = nullptr,
+                          u64 ref = 0, int* rank = nullptr) {
   constexpr int VEC = VECTOR ? Vec16<T>::N : 1;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   u64 best = 0;
+  int cnt = 0;
   if constexpr (VECTOR) {
     // the row in chunks of at most BPD_BUF bytes: one bulk copy each, then a scan of the
     // staged vectors from shared memory
@@ -172,6 +214,12 @@ __device__ int row_argmax(const char* row, int V, RowStage& st, u64* red, int* s
         const uint4 q = v[i];
         const float m = VecMax<T>::finish(VecMax<T>::fold(q, VecMax<T>::NEG));
         if (m > bv || bi < 0) { bv = m; bi = c0 + i; bq = q; }
+        if constexpr (RANK) {
+          float x[VEC];
+          Vec16<T>::unpack(q, x);
+#pragma unroll
+          for (int e2 = 0; e2 < VEC; ++e2) cnt += make_key(x[e2], static_cast<u32>((c0 + i) * VEC + e2)) > ref ? 1 : 0;
+        }
       }
     }
     if (bi >= 0) {
@@ -186,17 +234,27 @@ __device__ int row_argmax(const char* row, int V, RowStage& st, u64* red, int* s
     for (int i = tid; i < V; i += BPD_RT) {
       const u64 k = make_key(Elem<T>::load(row, i), static_cast<u32>(i));
       best = k > best ? k : best;
+      if constexpr (RANK) cnt += k > ref ? 1 : 0;
     }
   }
   best = warp_max_u64(best);
-  if (lane == 0) red[warp] = best;
+  if constexpr (RANK) cnt = __reduce_add_sync(FULL, cnt);
+  if (lane == 0) {
+    red[warp] = best;
+    if constexpr (RANK) redc[warp] = cnt;
+  }
   __syncthreads();
   if (warp == 0) {
     u64 v = lane < BPD_RT / 32 ? red[lane] : 0ull;
     v = warp_max_u64(v);
+    if constexpr (RANK) {
+      const int cc = __reduce_add_sync(FULL, lane < BPD_RT / 32 ? redc[lane] : 0);
+      if (lane == 0) redc[BPD_RT / 32] = cc;
+    }
     if (lane == 0) red[BPD_RT / 32] = v;
   }
   __syncthreads();
+  if constexpr (RANK) *rank = redc[BPD_RT / 32];
   return static_cast<int>(key_v(red[BPD_RT / 32]));
 }
 
@@ -237,12 +295,14 @@ __device__ __forceinline__ void prefetch_row_l2(const char* p, int64_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p), "r"(static_cast<unsigned>(bytes)) : "memory");
 }
 
-template <typename T, bool VECTOR>
+template <typename T, bool VECTOR, bool RANK>
 __global__ void __launch_bounds__(BPD_RT, 3) bpd_verify_queue_kernel(const void* logits, const int32_t* proposals, int B,
-                                                                  int k, int V, int eos, int32_t* khat_out,
-                                                                  int32_t* next_out, int* status) {
+                                                                  int k, int V, int eos, BpdCrit crit,
+                                                                  int32_t* khat_out, int32_t* next_out, int* status) {
   extern __shared__ __align__(128) unsigned char bpd_smem[];
   __shared__ u64 red[BPD_RT / 32 + 1];
+  __shared__ int redc[BPD_RT / 32 + 1];
+  __shared__ u64 s_ref;
   __shared__ __align__(8) u64 bar;
   __shared__ int s_unit, s_b, s_h, s_q;
   const int tid = threadIdx.x;
@@ -268,16 +328,33 @@ __global__ void __launch_bounds__(BPD_RT, 3) bpd_verify_queue_kernel(const void*
     if (eos >= 0)
       for (int e = 0; e < k; ++e)
         if (__ldg(props + e) == eos) { checks = min(checks, e); break; }
-    int n = 1, am = -1;
+    int n = 1, am = -1, last = -1;
     for (int p = 0; p < checks; ++p) {
+      const char* row = base + static_cast<int64_t>(p) * k * row_bytes;
       // the next head-0 row is read unless this check fails: start it towards L2
       if (VECTOR && tid == 0 && p + 1 <= checks)
         prefetch_row_l2(base + static_cast<int64_t>(p + 1) * k * row_bytes, row_bytes);
-      am = row_argmax<T, VECTOR>(base + static_cast<int64_t>(p) * k * row_bytes, V, st, red, status);
-      if (__ldg(props + p + 1) != am) break;
+      const int prop = __ldg(props + p + 1);
+      int rank = 0;
+      if constexpr (RANK) {
+        if (tid == 0) s_ref = token_key<T>(row, prop, V);
+        __syncthreads();
+        am = row_argmax<T, VECTOR, true>(row, V, st, red, status, redc, s_ref, &rank);
+      } else {
+        am = row_argmax<T, VECTOR>(row, V, st, red, status);
+      }
+      last = p;
+      if (!bpd_passes(crit, prop, am, rank, V)) break;
       ++n;
     }
-    if (n - 1 == checks)                           // khat - 1 not read by the checks: head 0 there
+    // the minimum block (§5.3), then the EOS cut: proposals past an EOS are not accepted
+    if (crit.min_accept > n) {
+      n = min(crit.min_accept, k);
+      if (eos >= 0)
+        for (int e = 0; e < n; ++e)
+          if (__ldg(props + e) == eos) { n = e + 1; break; }
+    }
+    if (last != n - 1)                             // khat - 1 not read by the checks: head 0 there
       am = row_argmax<T, VECTOR>(base + static_cast<int64_t>(n - 1) * k * row_bytes, V, st, red, status);
     if (tid == 0) {
       khat_out[b] = n;
@@ -361,40 +438,45 @@ int launch_bpd_propose(const void* logits, int B, int k, int V, int dtype, bool 
   return cudaGetLastError() == cudaSuccess ? VBS_OK : VBS_ECUDA;
 }
 
-template <typename T, bool VECTOR>
+template <typename T, bool VECTOR, bool RANK>
 static int launch_queue(int grid, const void* logits, const int32_t* proposals, int B, int k, int V, int eos,
-                        int32_t* khat, int32_t* next, int* status, cudaStream_t s) {
+                        const BpdCrit& crit, int32_t* khat, int32_t* next, int* status, cudaStream_t s) {
   const int smem = VECTOR ? BPD_BUF : 0;
   static bool attr_set = false;                  // one per kernel instantiation
   if (VECTOR && !attr_set) {
-    if (cudaFuncSetAttribute(bpd_verify_queue_kernel<T, VECTOR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(bpd_verify_queue_kernel<T, VECTOR, RANK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              BPD_BUF) != cudaSuccess)
       return VBS_ECUDA;
     attr_set = true;
   }
-  bpd_verify_queue_kernel<T, VECTOR><<<grid, BPD_RT, smem, s>>>(logits, proposals, B, k, V, eos, khat, next, status);
+  bpd_verify_queue_kernel<T, VECTOR, RANK><<<grid, BPD_RT, smem, s>>>(logits, proposals, B, k, V, eos, crit, khat,
+                                                                     next, status);
+  return cudaGetLastError() == cudaSuccess ? VBS_OK : VBS_ECUDA;
+}
+
+template <typename T, bool VECTOR>
+static int launch_verify(const void* logits, const int32_t* proposals, int B, int k, int V, int eos,
+                         const BpdCrit& crit, int32_t* khat, int32_t* next, int* status, int num_sms, cudaStream_t s) {
+  const bool rank = crit.mode == VBS_BPD_TOPK;
+  if (B <= BPD_MAX_B) {
+    const int grid = std::min(B * k, num_sms * 3);  // three CTAs (three staged rows) per SM
+    return rank ? launch_queue<T, VECTOR, true>(grid, logits, proposals, B, k, V, eos, crit, khat, next, status, s)
+                : launch_queue<T, VECTOR, false>(grid, logits, proposals, B, k, V, eos, crit, khat, next, status, s);
+  }
+  if (rank) bpd_verify_kernel<T, VECTOR, true><<<B, BPD_NT, 0, s>>>(logits, proposals, k, V, eos, crit, khat, next);
+  else bpd_verify_kernel<T, VECTOR, false><<<B, BPD_NT, 0, s>>>(logits, proposals, k, V, eos, crit, khat, next);
   return cudaGetLastError() == cudaSuccess ? VBS_OK : VBS_ECUDA;
 }
 
 int launch_bpd_verify(const void* logits, const int32_t* proposals, int B, int k, int V, int dtype, bool vec_ok,
-                      int eos, int32_t* khat, int32_t* next, int* status, int num_sms, cudaStream_t s) {
+                      int eos, const BpdCrit& crit, int32_t* khat, int32_t* next, int* status, int num_sms,
+                      cudaStream_t s) {
   if (B == 0) return VBS_OK;
-  if (B <= BPD_MAX_B) {
-    const int grid = std::min(B * k, num_sms * 3);  // three CTAs (three staged rows) per SM
-    if (dtype == VBS_BF16)
-      return vec_ok ? launch_queue<bf16_t, true>(grid, logits, proposals, B, k, V, eos, khat, next, status, s)
-                    : launch_queue<bf16_t, false>(grid, logits, proposals, B, k, V, eos, khat, next, status, s);
-    return vec_ok ? launch_queue<float, true>(grid, logits, proposals, B, k, V, eos, khat, next, status, s)
-                  : launch_queue<float, false>(grid, logits, proposals, B, k, V, eos, khat, next, status, s);
-  }
-  if (dtype == VBS_BF16) {
-    if (vec_ok) bpd_verify_kernel<bf16_t, true><<<B, BPD_NT, 0, s>>>(logits, proposals, k, V, eos, khat, next);
-    else bpd_verify_kernel<bf16_t, false><<<B, BPD_NT, 0, s>>>(logits, proposals, k, V, eos, khat, next);
-  } else {
-    if (vec_ok) bpd_verify_kernel<float, true><<<B, BPD_NT, 0, s>>>(logits, proposals, k, V, eos, khat, next);
-    else bpd_verify_kernel<float, false><<<B, BPD_NT, 0, s>>>(logits, proposals, k, V, eos, khat, next);
-  }
-  return cudaGetLastError() == cudaSuccess ? VBS_OK : VBS_ECUDA;
+  if (dtype == VBS_BF16)
+    return vec_ok ? launch_verify<bf16_t, true>(logits, proposals, B, k, V, eos, crit, khat, next, status, num_sms, s)
+                  : launch_verify<bf16_t, false>(logits, proposals, B, k, V, eos, crit, khat, next, status, num_sms, s);
+  return vec_ok ? launch_verify<float, true>(logits, proposals, B, k, V, eos, crit, khat, next, status, num_sms, s)
+                : launch_verify<float, false>(logits, proposals, B, k, V, eos, crit, khat, next, status, num_sms, s);
 }
 
 }  // namespace vbs

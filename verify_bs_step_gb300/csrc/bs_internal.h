@@ -100,10 +100,15 @@ int launch_kv_naive(const KvGeom& g, const void* src, void* dst, const int32_t* 
 int launch_kv_paged_remap(const PagedArgs& a, const int32_t* beam_idx, int t_valid, cudaStream_t s);
 int launch_kv_paged_cow(const PagedArgs& a, bool bulk_ok, int num_sms, cudaStream_t s);
 
-// blockwise parallel decoding
+// blockwise parallel decoding; mode VBS_BPD_EXACT / _TOPK / _DISTANCE with its parameter,
+// and the minimum accepted block (1 = none)
+struct BpdCrit {
+  int mode, param, min_accept;
+};
 int launch_bpd_propose(const void* logits, int B, int k, int V, int dtype, bool vec_ok, int32_t* proposals,
                        cudaStream_t s);
 int launch_bpd_verify(const void* logits, const int32_t* proposals, int B, int k, int V, int dtype, bool vec_ok,
-                      int eos, int32_t* khat, int32_t* next, int* status, int num_sms, cudaStream_t s);
+                      int eos, const BpdCrit& crit, int32_t* khat, int32_t* next, int* status, int num_sms,
+                      cudaStream_t s);
 
 }  // namespace vbs
