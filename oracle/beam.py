@@ -286,13 +286,15 @@ class BeamSearch:
         self.scores = scores.reshape(B, W).copy()
         return StepResult(beam_idx, tokens, scores, self.done.copy(), bool(self.done.all()), steps)
 
-    def finalize(self):
-        """Best hypothesis per sentence: (out_seqs [B, max_len+1], out_len [B], out_score [B]).
+    def finalize(self, n_return: int = 1):
+        """The best n_return hypotheses per sentence: (out_seqs [B * n, max_len+1],
+        out_len [B * n], out_score [B * n], hyps), sentence b's j-th best in row b * n + j.
 
         Live beams of sentences not done are added first, with |y| = steps run
-        (R3); the winner is the highest normalised score, ties to the latest
-        list entry (N2); the row is BOS + tokens, then EOS if shorter than
-        max_len + 1, then PAD (N3).
+        (R3); hypotheses rank by normalised score, ties to the latest list entry
+        (N2: [BS] sorts ascending, stably, and pops from the end, once per returned
+        sequence; [LM] returns the first num_return_sequences by normalised score);
+        each row is BOS + tokens, then EOS if shorter than max_len + 1, then PAD (N3).
         """
         B, W = self.B, self.W
         width = self.max_len + 1
@@ -303,19 +305,22 @@ class BeamSearch:
             for w in range(W):
                 row = b * W + w
                 hyps[b].add(self.seqs[row], float(self.scores[b, w]), self.t)
-        out = np.full((B, width), self.pad, dtype=np.int64)
-        out_len = np.zeros(B, dtype=np.int64)
-        out_score = np.zeros(B, dtype=np.float64)
+        nr = n_return
+        out = np.full((B * nr, width), self.pad, dtype=np.int64)
+        out_len = np.zeros(B * nr, dtype=np.int64)
+        out_score = np.zeros(B * nr, dtype=np.float64)
         for b in range(B):
             ranked = sorted(hyps[b].beams, key=lambda h: h.ns)   # stable: equal scores keep list order
-            best = ranked[-1]
-            n = len(best.tokens)
-            out[b, :n] = best.tokens
-            if n < width and self.eos >= 0:
-                out[b, n] = self.eos
-                n += 1
-            out_len[b] = n
-            out_score[b] = best.ns
+            for j in range(nr):
+                best = ranked.pop()
+                n = len(best.tokens)
+                row = b * nr + j
+                out[row, :n] = best.tokens
+                if n < width and self.eos >= 0:
+                    out[row, n] = self.eos
+                    n += 1
+                out_len[row] = n
+                out_score[row] = best.ns
         return out, out_len, out_score, hyps
 
 

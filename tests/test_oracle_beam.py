@@ -333,3 +333,30 @@ def test_finalize_rules():
     bs.scores[0] = [-4.0, -8.0]
     out, out_len, out_score, _ = bs.finalize()
     assert list(out[0]) == [9, 1, 2, 5, -1] and out_len[0] == 4 and out_score[0] == -0.5
+
+
+def test_finalize_returns_the_best_n_in_order():
+    bs = ob.BeamSearch(1, 2, 6, eos=5, alpha=1.0, lp_kind=ob.LP_POWER, max_len=4, bos=9, pad=-1)
+    bs.t = 4
+    bs.hyps[0].add((9, 1, 2), -1.5, 3)          # ns = -0.5, EOS hit at step 3
+    bs.seqs = [[9, 1, 2, 3, 4], [9, 2, 2, 2, 2]]
+    bs.scores[0] = [-2.0, -8.0]                  # live: ns = -0.5 joins (tie), -2 does not (set full)
+    out, out_len, out_score, _ = bs.finalize(2)
+    # both hypotheses tie at -0.5: the latest list entry first, then the earlier one
+    assert [list(r) for r in out] == [[9, 1, 2, 3, 4], [9, 1, 2, 5, -1]]
+    assert list(out_len) == [5, 4] and list(out_score) == [-0.5, -0.5]
+    one = bs.finalize(1)
+    assert list(one[0][0]) == list(out[0]) and one[1][0] == out_len[0]
+
+
+@pytest.mark.parametrize("es", [ob.ES_FALSE, ob.ES_TRUE, ob.ES_NEVER])
+def test_finalize_n_ranks_the_whole_finished_set(es):
+    _, bs = _tiny_run(es, seed=21)
+    W = bs.W
+    out, out_len, out_score, hyps = bs.finalize(W)
+    best1 = bs.finalize(1)
+    for b in range(bs.B):
+        rows = slice(b * W, (b + 1) * W)
+        assert (np.diff(out_score[rows]) <= 0).all()                 # best first
+        assert sorted(out_score[rows]) == sorted(h.ns for h in hyps[b].beams)
+        np.testing.assert_array_equal(out[b * W], best1[0][b])       # the first is the single best
