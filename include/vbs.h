@@ -139,6 +139,16 @@ int bs_step(vbs_bs* ctx, const void* logits, int64_t ld, float* scores, int32_t*
  */
 int bs_finalize(vbs_bs* ctx, const float* scores, const int32_t* seqs, int32_t* out_seqs, int32_t* out_len,
                 float* out_score);
+/*
+ * bs_finalize returning the best n_return (1..W) hypotheses of every sentence
+ * ([LM] §9.2.2: the first num_return_sequences by normalised score; [BS] pops
+ * them from a stable ascending sort, so equal scores go latest-inserted
+ * first).  Sentence b's j-th best is row b * n_return + j of out_seqs
+ * [batch * n_return, max_len+1], out_len and out_score.  bs_finalize is the
+ * n_return = 1 case.  Errors: VBS_EINVAL for n_return outside 1..W.
+ */
+int bs_finalize_n(vbs_bs* ctx, const float* scores, const int32_t* seqs, int n_return, int32_t* out_seqs,
+                  int32_t* out_len, float* out_score);
 
 /*
  * Copy the finished sets out (device buffers, for inspection):

@@ -202,15 +202,18 @@ def run_gpu_case(case: BeamCase, tr: OracleTrace, device="cuda", check_every_ste
     return bs
 
 
-def compare_finalize(case, tr: OracleTrace, bs):
-    out, out_len, out_score = bs.finalize()
-    ref_out, ref_len, ref_score, _ = tr.bs.finalize()
+def compare_finalize(case, tr: OracleTrace, bs, n_return: int = 1):
+    out, out_len, out_score = bs.finalize(n_return)
+    ref_out, ref_len, ref_score, _ = tr.bs.finalize(n_return)
     out, out_len, out_score = out.cpu().numpy(), out_len.cpu().numpy(), out_score.cpu().numpy()
     T = len(tr.steps)
+    n = n_return
     for i, b in enumerate(tr.checked):
-        np.testing.assert_array_equal(out[b], ref_out[i], err_msg=f"final row sentence {b}")
-        assert out_len[b] == ref_len[i]
-        if math.isfinite(ref_score[i]):
-            assert abs(out_score[b] - ref_score[i]) <= score_tol(ref_score[i], T) + 1e-7 * abs(ref_score[i])
-        else:
-            assert out_score[b] == ref_score[i]
+        for j in range(n):
+            g, o = b * n + j, i * n + j
+            np.testing.assert_array_equal(out[g], ref_out[o], err_msg=f"final row sentence {b} rank {j}")
+            assert out_len[g] == ref_len[o]
+            if math.isfinite(ref_score[o]):
+                assert abs(out_score[g] - ref_score[o]) <= score_tol(ref_score[o], T) + 1e-7 * abs(ref_score[o])
+            else:
+                assert out_score[g] == ref_score[o]

@@ -31,6 +31,8 @@ def _run(case, finalize=True, every=True):
     bs = hz.run_gpu_case(case, tr, check_every_step=every)
     if finalize:
         hz.compare_finalize(case, tr, bs)
+        if case.W > 1:
+            hz.compare_finalize(case, tr, bs, n_return=case.W)     # every hypothesis, best first
     bs.close()
     return tr
 

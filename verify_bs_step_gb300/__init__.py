@@ -37,6 +37,7 @@ SIGNATURES = {
     "bs_reset": (_c_int, [_vp, _vp, _vp]),
     "bs_step": (_c_int, [_vp, _vp, _c_i64, _vp, _vp, _vp, _vp, _vp]),
     "bs_finalize": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp]),
+    "bs_finalize_n": (_c_int, [_vp, _vp, _vp, _c_int, _vp, _vp, _vp]),
     "bs_finished": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "bs_seqs": (_c_int, [_vp, _pp]),
     "bs_steps": (_c_int, [_vp, ctypes.POINTER(_c_int)]),
@@ -170,14 +171,21 @@ class BeamSearch:
                                    _vp(self.all_done.data_ptr()), kv.ctx, t_valid), "bs_step_paged")
         return self.beam_idx, self.tokens, self.scores
 
-    def finalize(self):
-        """(out_seqs [batch, max_len+1] int32, out_len [batch] int32, out_score [batch] fp32)."""
-        out = torch.empty(self.batch, self.max_len + 1, dtype=torch.int32, device=self.device)
-        out_len = torch.empty(self.batch, dtype=torch.int32, device=self.device)
-        out_score = torch.empty(self.batch, dtype=torch.float32, device=self.device)
-        _check(lib().bs_finalize(self.ctx, _vp(self.scores.data_ptr()), _vp(self.seqs.data_ptr()),
-                                 _vp(out.data_ptr()), _vp(out_len.data_ptr()), _vp(out_score.data_ptr())),
-               "bs_finalize")
+    def finalize(self, n_return: int = 1):
+        """(out_seqs [batch * n, max_len+1] int32, out_len [batch * n] int32, out_score [batch * n] fp32):
+        the best n_return hypotheses of each sentence, best first (sentence b's j-th in row b * n + j)."""
+        rows = self.batch * n_return
+        out = torch.empty(rows, self.max_len + 1, dtype=torch.int32, device=self.device)
+        out_len = torch.empty(rows, dtype=torch.int32, device=self.device)
+        out_score = torch.empty(rows, dtype=torch.float32, device=self.device)
+        if n_return == 1:
+            _check(lib().bs_finalize(self.ctx, _vp(self.scores.data_ptr()), _vp(self.seqs.data_ptr()),
+                                     _vp(out.data_ptr()), _vp(out_len.data_ptr()), _vp(out_score.data_ptr())),
+                   "bs_finalize")
+        else:
+            _check(lib().bs_finalize_n(self.ctx, _vp(self.scores.data_ptr()), _vp(self.seqs.data_ptr()), n_return,
+                                       _vp(out.data_ptr()), _vp(out_len.data_ptr()), _vp(out_score.data_ptr())),
+                   "bs_finalize_n")
         return out, out_len, out_score
 
     def finished(self):

@@ -259,16 +259,22 @@ VBS_EXPORT int bs_step(vbs_bs* c, const void* logits, int64_t ld, float* scores,
   return VBS_OK;
 }
 
-VBS_EXPORT int bs_finalize(vbs_bs* c, const float* scores, const int32_t* seqs, int32_t* out_seqs, int32_t* out_len,
-                           float* out_score) {
+VBS_EXPORT int bs_finalize_n(vbs_bs* c, const float* scores, const int32_t* seqs, int n_return, int32_t* out_seqs,
+                             int32_t* out_len, float* out_score) {
   if (!c || !scores || !out_seqs || !out_len || !out_score) return VBS_EINVAL;
+  if (n_return < 1 || n_return > c->a.W) return VBS_EINVAL;
   if (!c->reset_done) return VBS_ESTATE;
   const int32_t* sq = seqs ? seqs : c->own_seqs;
   if (sq != c->seqs_bound) return VBS_ESTATE;
   vbs::BsArgs a = c->a;
   a.t = c->step;
   a.lp_t = length_penalty(a.t, a.alpha, a.lp_kind);
-  return vbs::launch_bs_finalize(a, scores, sq, out_seqs, out_len, out_score, c->stream);
+  return vbs::launch_bs_finalize(a, scores, sq, n_return, out_seqs, out_len, out_score, c->stream);
+}
+
+VBS_EXPORT int bs_finalize(vbs_bs* c, const float* scores, const int32_t* seqs, int32_t* out_seqs, int32_t* out_len,
+                           float* out_score) {
+  return bs_finalize_n(c, scores, seqs, 1, out_seqs, out_len, out_score);
 }
 
 VBS_EXPORT int bs_finished(vbs_bs* c, int32_t* count, double* ns, int32_t* len, int32_t* serial, int32_t* tokens,

@@ -77,7 +77,7 @@ struct BsArgs {
 int launch_bs_step(const BsArgs& a, int grid, bool vector_ok, cudaStream_t s);
 bool bs_can_fuse_remap(const BsArgs& a, const PagedArgs& kv);
 int launch_bs_reset(const BsArgs& a, cudaStream_t s);
-int launch_bs_finalize(const BsArgs& a, const float* scores, const int32_t* seqs, int32_t* out_seqs,
+int launch_bs_finalize(const BsArgs& a, const float* scores, const int32_t* seqs, int n_ret, int32_t* out_seqs,
                        int32_t* out_len, float* out_score, cudaStream_t s);
 constexpr int BS_NSLOT = 4;       // row segments one stream CTA holds (cluster mode: W / C <= this)
 int bs_threads_per_cta();

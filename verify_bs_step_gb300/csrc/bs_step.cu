@@ -1307,11 +1307,11 @@ __global__ void bs_reset_kernel(const BsArgs a) {
 // One CTA per sentence: add the live beams of unfinished sentences (|y| = steps
 // run, normalised by lp_t = lp(steps run)), pick the best normalised score
 // (ties: the latest list entry), write the row.
-__global__ void bs_finalize_kernel(const BsArgs a, const float* scores, const int32_t* seqs,
+__global__ void bs_finalize_kernel(const BsArgs a, const float* scores, const int32_t* seqs, int n_ret,
                                    int32_t* out_seqs, int32_t* out_len, float* out_score) {
   __shared__ double f_ns[WMAX];
   __shared__ int f_serial[WMAX], f_src[WMAX], f_ntok[WMAX];
-  __shared__ int s_best;
+  __shared__ int s_order[WMAX];
   const int b = blockIdx.x;
   const int W = a.W, r0 = b * W, T = a.t, ld = a.seq_ld;
   if (threadIdx.x == 0) {
@@ -1348,24 +1348,37 @@ __global__ void bs_finalize_kernel(const BsArgs a, const float* scores, const in
         }
       }
     }
-    int best = 0;
-    for (int q = 1; q < count; ++q)
-      if (f_ns[q] > f_ns[best] || (f_ns[q] == f_ns[best] && f_serial[q] > f_serial[best])) best = q;
-    s_best = best;
-    out_score[b] = static_cast<float>(f_ns[best]);
-    const int n = f_ntok[best];
-    out_len[b] = (n < ld && a.eos >= 0) ? n + 1 : n;
+    // the n_ret best by (normalised score desc, insertion order desc): the j-th takes the best
+    // of the slots not yet taken
+    unsigned taken = 0u;
+    for (int j = 0; j < n_ret; ++j) {
+      int best = -1;
+      for (int q = 0; q < count; ++q) {
+        if (taken >> q & 1u) continue;
+        if (best < 0 || f_ns[q] > f_ns[best] || (f_ns[q] == f_ns[best] && f_serial[q] > f_serial[best])) best = q;
+      }
+      if (best < 0) best = 0;                         // fewer hypotheses than n_ret: never with n_ret <= W
+      taken |= 1u << best;
+      s_order[j] = best;
+      const int row = b * n_ret + j;
+      out_score[row] = static_cast<float>(f_ns[best]);
+      const int n = f_ntok[best];
+      out_len[row] = (n < ld && a.eos >= 0) ? n + 1 : n;
+    }
   }
   __syncthreads();
-  const int q = s_best;
-  const int n = f_ntok[q];
-  const int32_t* src = f_src[q] >= 0 ? seqs + static_cast<int64_t>(f_src[q]) * ld
-                                     : a.fin_tok + static_cast<int64_t>(r0 + q) * ld;
-  for (int c = threadIdx.x; c < ld; c += blockDim.x) {
-    int v = a.pad;
-    if (c < n) v = src[c];
-    else if (c == n && a.eos >= 0) v = a.eos;
-    out_seqs[static_cast<int64_t>(b) * ld + c] = v;
+  for (int j = 0; j < n_ret; ++j) {
+    const int q = s_order[j];
+    const int n = f_ntok[q];
+    const int32_t* src = f_src[q] >= 0 ? seqs + static_cast<int64_t>(f_src[q]) * ld
+                                       : a.fin_tok + static_cast<int64_t>(r0 + q) * ld;
+    int32_t* dst = out_seqs + (static_cast<int64_t>(b) * n_ret + j) * ld;
+    for (int c = threadIdx.x; c < ld; c += blockDim.x) {
+      int v = a.pad;
+      if (c < n) v = src[c];
+      else if (c == n && a.eos >= 0) v = a.eos;
+      dst[c] = v;
+    }
   }
 }
 
@@ -1464,9 +1477,9 @@ int launch_bs_reset(const BsArgs& a, cudaStream_t s) {
   return cudaGetLastError() == cudaSuccess ? VBS_OK : VBS_ECUDA;
 }
 
-int launch_bs_finalize(const BsArgs& a, const float* scores, const int32_t* seqs, int32_t* out_seqs,
+int launch_bs_finalize(const BsArgs& a, const float* scores, const int32_t* seqs, int n_ret, int32_t* out_seqs,
                        int32_t* out_len, float* out_score, cudaStream_t s) {
-  bs_finalize_kernel<<<a.B, 128, 0, s>>>(a, scores, seqs, out_seqs, out_len, out_score);
+  bs_finalize_kernel<<<a.B, 128, 0, s>>>(a, scores, seqs, n_ret, out_seqs, out_len, out_score);
   return cudaGetLastError() == cudaSuccess ? VBS_OK : VBS_ECUDA;
 }
 
