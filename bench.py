@@ -447,8 +447,10 @@ def run_extras(args, torch, vbs, synth, dev, stream, peak):
     extra = {}
     with torch.cuda.stream(stream):
         # -- bs_step alone, Llama and T-base shapes --------------------------------------
+        # bs_step_two_pass_llama: the two-pass coarse-selection ablation on the same workload
         for name, kind, B, W, V, T in (("bs_step_llama", "llama", 64, 4, 128256, 200),
-                                       ("bs_step_tbase", "tbase", 128, 4, 32000, 64)):
+                                       ("bs_step_tbase", "tbase", 128, 4, 32000, 64),
+                                       ("bs_step_two_pass_llama", "llama", 64, 4, 128256, 200)):
             R = B * W
             n = max(RING, -(-4 * 129_000_000 // (R * V * 2)) + 1)
             if kind == "llama":
@@ -462,18 +464,19 @@ def run_extras(args, torch, vbs, synth, dev, stream, peak):
             a_ = [vp(bs.scores.data_ptr()), vp(bs.seqs.data_ptr()), vp(bs.beam_idx.data_ptr()),
                   vp(bs.tokens.data_ptr()), vp(bs.all_done.data_ptr())]
             prs = [vp(x.data_ptr()) for x in ring]
+            step_fn = L_.bs_step_two_pass if name.startswith("bs_step_two_pass") else L_.bs_step
             ts, i = [], 0
             while len(ts) < 400:
                 # one decode: the first step (only beam 0 of each sentence is live) is not timed
                 L_.bs_reset(bs.ctx, a_[0], a_[1])
-                L_.bs_step(bs.ctx, prs[i % n], V, *a_)
+                step_fn(bs.ctx, prs[i % n], V, *a_)
                 i += 1
                 evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                        for _ in range(T - 1)]
                 torch.cuda._sleep(int(2e5) * (T - 1))      # the host queues the decode ahead of the GPU
                 for e_a, e_b in evs:
                     e_a.record(stream)
-                    L_.bs_step(bs.ctx, prs[i % n], V, *a_)
+                    step_fn(bs.ctx, prs[i % n], V, *a_)
                     e_b.record(stream)
                     i += 1
                 torch.cuda.synchronize()
@@ -484,6 +487,8 @@ def run_extras(args, torch, vbs, synth, dev, stream, peak):
             extra[name] = {"B": B, "W": W, "V": V, "avg_us": round(avg * 1e3, 3),
                            "steps_per_s": round(1e3 / avg, 1), "achieved_gbs": round(byts / (avg / 1e3) / 1e9, 1),
                            "frac_of_peak": round(byts / (avg / 1e3) / 1e9 / peak, 4), "bytes": byts}
+            if step_fn is not L_.bs_step:
+                extra[name]["logit_bytes_read"] = 2 * R * V * 2       # two passes over the logits
             bs.close()
             del ring
         # -- naive KV gather at the Llama shape (t_valid = 1000) ---------------------------

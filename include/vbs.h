@@ -125,6 +125,16 @@ int bs_reset(vbs_bs* ctx, float* scores, int32_t* seqs);
  */
 int bs_step(vbs_bs* ctx, const void* logits, int64_t ld, float* scores, int32_t* seqs, int32_t* beam_idx,
             int32_t* tokens, int32_t* all_done);
+/*
+ * bs_step through the two-pass coarse selection of [LS] (an ablation, same
+ * arguments and results): a first pass over each row computes its log-sum-exp
+ * and R = the smallest of K group maxima (at most the row's K-th largest
+ * logit; K = 2W), a second pass reads the row again and keeps the K best keys
+ * among the logits >= R, then the per-sentence merge of bs_step runs.  It reads
+ * the logits twice; bs_step reads them once.
+ */
+int bs_step_two_pass(vbs_bs* ctx, const void* logits, int64_t ld, float* scores, int32_t* seqs, int32_t* beam_idx,
+                     int32_t* tokens, int32_t* all_done);
 
 /*
  * Final choice ([BS] after the loop): the live beams of every sentence not yet

@@ -180,8 +180,9 @@ def compare_finished(case, tr: OracleTrace, fin: dict, t: int):
                 assert ns[r] == hy.ns
 
 
-def run_gpu_case(case: BeamCase, tr: OracleTrace, device="cuda", check_every_step=True):
-    """Run the CUDA path over the oracle's steps and compare everything; returns the BeamSearch."""
+def run_gpu_case(case: BeamCase, tr: OracleTrace, device="cuda", check_every_step=True, two_pass=False):
+    """Run the CUDA path over the oracle's steps and compare everything; returns the BeamSearch.
+    With two_pass, every step goes through the two-pass coarse-selection ablation."""
     import verify_bs_step_gb300 as vbs
 
     bias_dev = synth.zipf_bias(case.V, case.seed, device) if case.kind == "llama" else None
@@ -191,7 +192,8 @@ def run_gpu_case(case: BeamCase, tr: OracleTrace, device="cuda", check_every_ste
                         bos=case.bos, pad=case.pad, dtype=case.dtype, device=device)
     for t in range(1, len(tr.steps) + 1):
         logits = step_logits(case, t, tr.salts[t - 1], device, bias_dev, bias_cpu)
-        bi, tok, sc = bs.step(logits[:, :case.V] if case.ld_pad else logits)
+        lg = logits[:, :case.V] if case.ld_pad else logits
+        bi, tok, sc = bs.step_two_pass(lg) if two_pass else bs.step(lg)
         if check_every_step or t == len(tr.steps):
             torch.cuda.synchronize()
             compare_step(case, tr, t, bi.cpu().numpy(), tok.cpu().numpy(), sc.cpu().numpy(),

@@ -257,3 +257,30 @@ def test_sweep_grid(B, W, V, dtype):
     case = hz.BeamCase("sweep", B, W, V, steps, dtype, eos=11, alpha=0.6, seed=B + W + V,
                        checked=checked)
     _run(case, every=not big)
+
+
+# ------------------------------------------------------------------------------------
+# the two-pass coarse-selection ablation (bs_step_two_pass) against the same oracle
+# ------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("kind,B,W,V,T,dtype,eos,ld_pad", [
+    ("tiny", 3, 2, 6, 8, torch.float32, 5, 0),
+    ("sweep", 32, 4, 32000, 20, torch.bfloat16, 7, 0),
+    ("sweep", 4, 16, 4096, 12, torch.float32, 3, 0),        # K = 32
+    ("sweep", 5, 3, 1003, 12, torch.bfloat16, 2, 0),        # element path
+    ("sweep", 2, 4, 4096, 10, torch.float32, 1, 5),         # row stride ld > V
+    ("ramp", 2, 4, 32000, 4, torch.float32, 5, 0),          # many logits above the first bar
+])
+def test_two_pass_ablation_matches_oracle(kind, B, W, V, T, dtype, eos, ld_pad):
+    case = hz.BeamCase(kind, B, W, V, T, dtype, eos=eos, alpha=0.6, seed=B * 13 + V % 101, ld_pad=ld_pad)
+    tr = hz.run_oracle(case)
+    bs = hz.run_gpu_case(case, tr, two_pass=True)
+    hz.compare_finalize(case, tr, bs)
+    bs.close()
+
+
+def test_two_pass_ablation_llama_shape():
+    case = hz.BeamCase("llama", 64, 4, 128256, 3, torch.bfloat16, eos=2, alpha=0.6, seed=1236, checked=[0, 17, 63])
+    tr = hz.run_oracle(case)
+    bs = hz.run_gpu_case(case, tr, two_pass=True)
+    bs.close()

@@ -50,6 +50,7 @@ SIGNATURES = {
     "kv_paged_prefill": (_c_int, [_vp, _c_int]),
     "kv_paged_prepare": (_c_int, [_vp, _c_int]),
     "kv_paged_reorder": (_c_int, [_vp, _vp, _c_int]),
+    "bs_step_two_pass": (_c_int, [_vp, _vp, _c_i64, _vp, _vp, _vp, _vp, _vp]),
     "bs_step_paged": (_c_int, [_vp, _vp, _c_i64, _vp, _vp, _vp, _vp, _vp, _vp, _c_int]),
     "kv_paged_copy": (_c_int, [_vp]),
     "kv_paged_table": (_c_int, [_vp, _pp, ctypes.POINTER(_c_int)]),
@@ -156,6 +157,18 @@ class BeamSearch:
         _check(lib().bs_step(self.ctx, _dev_ptr(logits, "logits"), logits.stride(0), _vp(self.scores.data_ptr()),
                              _vp(self.seqs.data_ptr()), _vp(self.beam_idx.data_ptr()),
                              _vp(self.tokens.data_ptr()), _vp(self.all_done.data_ptr())), "bs_step")
+        return self.beam_idx, self.tokens, self.scores
+
+    def step_two_pass(self, logits: torch.Tensor):
+        """step() through the two-pass coarse-selection ablation (reads the logits twice)."""
+        if logits.dim() != 2 or logits.shape[0] != self.R or logits.shape[1] != self.V or logits.stride(1) != 1:
+            raise ValueError(f"logits must be [{self.R}, {self.V}] with unit stride along V")
+        if logits.dtype != self.dtype:
+            raise ValueError(f"logits must be {self.dtype}")
+        _check(lib().bs_step_two_pass(self.ctx, _dev_ptr(logits, "logits"), logits.stride(0),
+                                      _vp(self.scores.data_ptr()), _vp(self.seqs.data_ptr()),
+                                      _vp(self.beam_idx.data_ptr()), _vp(self.tokens.data_ptr()),
+                                      _vp(self.all_done.data_ptr())), "bs_step_two_pass")
         return self.beam_idx, self.tokens, self.scores
 
     def step_paged(self, logits: torch.Tensor, kv: "PagedKV", t_valid: int):

@@ -156,8 +156,8 @@ VBS_EXPORT int bs_init(vbs_bs** out, int batch, int W, int V, int eos, double al
     a.part_M = cv.take<float>(R * a.P);
     a.part_l = cv.take<float>(R * a.P);
     a.part_key = cv.take<u64>(R * a.P * a.K);
-    a.row_lse = cv.take<double>(R);
-    a.row_key = cv.take<u64>(R * a.K);
+    a.rtopk_bar = cv.take<unsigned>(R);
+    a.row_one = cv.take<int>(R);
     a.row_p0 = cv.take<int>(R);
     a.row_np = cv.take<int>(R);
     a.done_count = cv.take<int>(1);
@@ -193,6 +193,8 @@ VBS_EXPORT int bs_init(vbs_bs** out, int batch, int W, int V, int eos, double al
   bool ok = cudaMemsetAsync(c->dev_block, 0, cv.off, c->stream) == cudaSuccess;
   ok = ok && cudaMemcpyAsync(a.row_p0, p0.data(), R * sizeof(int), cudaMemcpyHostToDevice, c->stream) == cudaSuccess;
   ok = ok && cudaMemcpyAsync(a.row_np, np.data(), R * sizeof(int), cudaMemcpyHostToDevice, c->stream) == cudaSuccess;
+  const std::vector<int> ones(R, 1);
+  ok = ok && cudaMemcpyAsync(a.row_one, ones.data(), R * sizeof(int), cudaMemcpyHostToDevice, c->stream) == cudaSuccess;
   ok = ok && cudaStreamSynchronize(c->stream) == cudaSuccess;
   if (!ok) {
     cudaFree(c->dev_block);
@@ -254,6 +256,18 @@ VBS_EXPORT int bs_step(vbs_bs* c, const void* logits, int64_t ld, float* scores,
   int st = step_args(c, logits, ld, scores, seqs, beam_idx, tokens, all_done, a, vec_ok);
   if (st != VBS_OK) return st;
   st = vbs::launch_bs_step(a, c->grid, vec_ok, c->stream);
+  if (st != VBS_OK) return st;
+  c->step += 1;
+  return VBS_OK;
+}
+
+VBS_EXPORT int bs_step_two_pass(vbs_bs* c, const void* logits, int64_t ld, float* scores, int32_t* seqs,
+                                int32_t* beam_idx, int32_t* tokens, int32_t* all_done) {
+  vbs::BsArgs a;
+  bool vec_ok = false;
+  int st = step_args(c, logits, ld, scores, seqs, beam_idx, tokens, all_done, a, vec_ok);
+  if (st != VBS_OK) return st;
+  st = vbs::launch_bs_step_two_pass(a, vec_ok, c->stream);
   if (st != VBS_OK) return st;
   c->step += 1;
   return VBS_OK;

@@ -52,8 +52,8 @@ struct BsArgs {
   float* part_M;
   float* part_l;
   unsigned long long* part_key;
-  double* row_lse;
-  unsigned long long* row_key;
+  unsigned* rtopk_bar;            // [R] the two-pass ablation's per-row bar (ordered logit bits)
+  int* row_one;                   // [R] all 1: the two-pass ablation writes one partial slot per row
   int* row_p0;                    // [R] the first CTA whose range holds row r
   int* row_np;                    // [R] the number of CTAs (partials) holding row r
   int* done_count;                // sentences finished (step-local counter)
@@ -76,6 +76,7 @@ struct BsArgs {
 
 int launch_bs_step(const BsArgs& a, int grid, bool vector_ok, cudaStream_t s);
 bool bs_can_fuse_remap(const BsArgs& a, const PagedArgs& kv);
+int launch_bs_step_two_pass(const BsArgs& a, bool vector_ok, cudaStream_t s);
 int launch_bs_reset(const BsArgs& a, cudaStream_t s);
 int launch_bs_finalize(const BsArgs& a, const float* scores, const int32_t* seqs, int n_ret, int32_t* out_seqs,
                        int32_t* out_len, float* out_score, cudaStream_t s);

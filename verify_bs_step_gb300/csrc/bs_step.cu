@@ -1450,6 +1450,179 @@ static int launch_cluster(const BsArgs& a, cudaStream_t s) {
   return cudaLaunchKernelEx(&cfg, bs_cluster_kernel<T, TMA, FUSE>, a) == cudaSuccess ? VBS_OK : VBS_ECUDA;
 }
 
+// ---------------------------------------------------------------------------------------
+// ablation: the two-pass coarse selection of the pages' LightSeq article (R-top-k)
+// ---------------------------------------------------------------------------------------
+//
+// The article's first pass over a row splits its logits into K groups, takes each group's
+// maximum and the smallest of those maxima, R (at most the row's K-th largest logit: the
+// K maxima are K distinct logits at or above R), together with the row's log-sum-exp;
+// the second pass reads the row again and queues every logit >= R; a sort of the queue
+// gives the exact top K.  Here the groups are the logits each thread reads, grouped by
+// thread index mod K (any split into K non-empty groups bounds the K-th largest; an empty
+// group makes R the lowest bar), the queue keeps the row's K best keys exactly (a pass that
+// overflows raises the bar to the K-th best key it holds, which only rises, and runs
+// again), and each row's (max, scaled sum, K best keys) goes to the partial slot the merge
+// kernel reads, so the rest of the step is the two-kernel path's merge.  The logits are
+// read twice: the path exists to measure that against the one-pass kernels.
+
+constexpr int RT_NT = 256;
+constexpr int RT_U = 4;
+constexpr int RT_CAP = 2048;
+
+template <typename T, bool VECTOR>
+__global__ void __launch_bounds__(RT_NT) rtopk_pass1_kernel(const BsArgs a) {
+  constexpr int VEC = VECTOR ? Vec16<T>::N : 1;
+  __shared__ float sM[RT_NT / 32], sl[RT_NT / 32];
+  __shared__ u32 gmax[KMAX];
+  const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int K = a.K;
+  if (tid < K) gmax[tid] = 0u;
+  __syncthreads();
+  if (row_skipped(a, r)) return;                    // the same for every thread of the row
+  const char* row = reinterpret_cast<const char*>(a.logits) + static_cast<int64_t>(r) * a.ld * Elem<T>::BYTES;
+  const int n = a.V / VEC;
+  float m = -INFINITY, M = -INFINITY, l = 0.f;
+  for (int i0 = tid; i0 < n; i0 += RT_NT * RT_U) {
+    float x[RT_U][VEC];
+#pragma unroll
+    for (int u = 0; u < RT_U; ++u) {
+      const int i = i0 + u * RT_NT;
+      if (i < n) {
+        if constexpr (VECTOR) Vec16<T>::unpack(ld_stream16(row + static_cast<int64_t>(i) * 16), x[u]);
+        else x[u][0] = Elem<T>::load(row, i);
+      } else {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) x[u][e] = -INFINITY;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < RT_U; ++u) {
+      float tm = x[u][0];
+#pragma unroll
+      for (int e = 1; e < VEC; ++e) tm = fmaxf(tm, x[u][e]);
+      if (tm > m) {
+        const float Mn = tm * LOG2E_F;
+        l *= ex2(M - Mn);
+        M = Mn;
+        m = tm;
+      }
+      if (tm > -INFINITY) {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) l += ex2(fmaf(x[u][e], LOG2E_F, -M));
+      }
+    }
+  }
+  if (m > -INFINITY) atomicMax(&gmax[tid % K], ord_f32(m));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float M2 = __shfl_xor_sync(FULL, M, off);
+    const float l2 = __shfl_xor_sync(FULL, l, off);
+    lse_merge(M, l, M2, l2);
+  }
+  if (lane == 0) { sM[warp] = M; sl[warp] = l; }
+  __syncthreads();
+  if (warp == 0) {
+    M = lane < RT_NT / 32 ? sM[lane] : -INFINITY;
+    l = lane < RT_NT / 32 ? sl[lane] : 0.f;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float M2 = __shfl_xor_sync(FULL, M, off);
+      const float l2 = __shfl_xor_sync(FULL, l, off);
+      lse_merge(M, l, M2, l2);
+    }
+    if (lane == 0) {
+      const int64_t slot = static_cast<int64_t>(r) * a.P;
+      a.part_M[slot] = M;
+      a.part_l[slot] = l;
+      u32 rb = gmax[0];
+      for (int g = 1; g < K; ++g) rb = min(rb, gmax[g]);
+      a.rtopk_bar[r] = rb;
+    }
+  }
+}
+
+template <typename T, bool VECTOR>
+__global__ void __launch_bounds__(RT_NT) rtopk_pass2_kernel(const BsArgs a) {
+  constexpr int VEC = VECTOR ? Vec16<T>::N : 1;
+  __shared__ u64 q[RT_CAP];
+  __shared__ u64 sel[KMAX];
+  __shared__ u64 bar;
+  __shared__ int cnt;
+  const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int K = a.K;
+  if (row_skipped(a, r)) return;
+  const char* row = reinterpret_cast<const char*>(a.logits) + static_cast<int64_t>(r) * a.ld * Elem<T>::BYTES;
+  const int n = a.V / VEC;
+  if (tid == 0) bar = static_cast<u64>(a.rtopk_bar[r]) << 32;
+  for (;;) {
+    if (tid == 0) cnt = 0;
+    __syncthreads();
+    const u64 b = bar;
+    for (int i0 = tid; i0 < n; i0 += RT_NT * RT_U) {
+      float x[RT_U][VEC];
+#pragma unroll
+      for (int u = 0; u < RT_U; ++u) {
+        const int i = i0 + u * RT_NT;
+        if (i < n) {
+          if constexpr (VECTOR) Vec16<T>::unpack(ld_stream16(row + static_cast<int64_t>(i) * 16), x[u]);
+          else x[u][0] = Elem<T>::load(row, i);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < RT_U; ++u) {
+        const int i = i0 + u * RT_NT;
+        if (i >= n) continue;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+          const u64 key = make_key(x[u][e], static_cast<u32>(i * VEC + e));
+          if (key >= b) {
+            const int pos = atomicAdd(&cnt, 1);
+            if (pos < RT_CAP) q[pos] = key;
+          }
+        }
+      }
+    }
+    __syncthreads();
+    const int c = cnt;
+    __syncthreads();                                // every thread has read the count
+    if (c <= RT_CAP) break;                         // the same for every thread
+    if (warp == 0) {
+      warp_select_topk(q, RT_CAP, K, sel, lane);
+      if (lane == 0) bar = sel[K - 1];
+    }
+    __syncthreads();
+  }
+  if (warp == 0) {
+    warp_select_topk(q, min(cnt, RT_CAP), K, sel, lane);
+    if (lane < K) a.part_key[static_cast<int64_t>(r) * a.P * K + lane] = sel[lane];
+  }
+}
+
+int launch_bs_step_two_pass(const BsArgs& a0, bool vector_ok, cudaStream_t s) {
+  BsArgs a = a0;
+  a.row_np = a.row_one;                             // one partial slot per row
+  if (a.dtype == VBS_BF16) {
+    if (vector_ok) {
+      rtopk_pass1_kernel<bf16_t, true><<<a.R, RT_NT, 0, s>>>(a);
+      rtopk_pass2_kernel<bf16_t, true><<<a.R, RT_NT, 0, s>>>(a);
+    } else {
+      rtopk_pass1_kernel<bf16_t, false><<<a.R, RT_NT, 0, s>>>(a);
+      rtopk_pass2_kernel<bf16_t, false><<<a.R, RT_NT, 0, s>>>(a);
+    }
+  } else {
+    if (vector_ok) {
+      rtopk_pass1_kernel<float, true><<<a.R, RT_NT, 0, s>>>(a);
+      rtopk_pass2_kernel<float, true><<<a.R, RT_NT, 0, s>>>(a);
+    } else {
+      rtopk_pass1_kernel<float, false><<<a.R, RT_NT, 0, s>>>(a);
+      rtopk_pass2_kernel<float, false><<<a.R, RT_NT, 0, s>>>(a);
+    }
+  }
+  if (cudaGetLastError() != cudaSuccess) return VBS_ECUDA;
+  return launch_merge(a, s);
+}
+
 int launch_bs_step(const BsArgs& a, int grid, bool vector_ok, cudaStream_t s) {
   if (a.cluster) {
     if (a.kv_fuse) {
