@@ -32,18 +32,24 @@ __device__ __forceinline__ bool bpd_passes(const BpdCrit& crit, int prop, int am
   return prop == am;
 }
 
-// The key of token `tok` in a row (0 for a token outside [0, V), which passes no rank test).
+// The logit of token `tok` in a row (any value for a token outside [0, V), which passes
+// no rank test).
 template <typename T>
-__device__ __forceinline__ u64 token_key(const char* row, int tok, int V) {
-  if (tok < 0 || tok >= V) return 0ull;
-  return make_key(Elem<T>::load(row, tok), static_cast<u32>(tok));
+__device__ __forceinline__ float token_value(const char* row, int tok, int V) {
+  return (tok >= 0 && tok < V) ? Elem<T>::load(row, tok) : 0.f;
+}
+
+// Whether element (x, v) ranks above the proposal (xp, prop): a larger logit, or an equal
+// one at a lower id.
+__device__ __forceinline__ int beats(float x, int v, float xp, int prop) {
+  return (x > xp || (x == xp && v < prop)) ? 1 : 0;
 }
 
 // Best key of the vectors [i0, i1) of one row, for this thread (strided by `stride`);
-// with RANK, *cnt also counts this thread's keys above `ref`.
+// with RANK, *cnt also counts this thread's elements that beat the proposal (xp, prop).
 template <typename T, bool VECTOR, bool RANK = false>
 __device__ __forceinline__ u64 thread_row_best(const char* row, int64_t i0, int64_t i1, int64_t stride,
-                                               u64 ref = 0, int* cnt = nullptr) {
+                                               float xp = 0.f, int prop = -1, int* cnt = nullptr) {
   constexpr int VEC = VECTOR ? Vec16<T>::N : 1;
   u64 best = 0;
   int c = 0;
@@ -69,7 +75,7 @@ __device__ __forceinline__ u64 thread_row_best(const char* row, int64_t i0, int6
         for (int e = 0; e < VEC; ++e) {
           u64 k = make_key(x[e], static_cast<u32>(i * VEC + e));
           best = k > best ? k : best;
-          if constexpr (RANK) c += k > ref ? 1 : 0;
+          if constexpr (RANK) c += beats(x[e], static_cast<int>(i * VEC + e), xp, prop);
         }
       }
     }
@@ -78,13 +84,14 @@ __device__ __forceinline__ u64 thread_row_best(const char* row, int64_t i0, int6
   return best;
 }
 
-// The row's argmax; with RANK also *rank = the number of keys above `ref` (every thread).
+// The row's argmax; with RANK also *rank = the number of elements that beat the proposal
+// (xp, prop) (every thread).
 template <typename T, bool VECTOR, bool RANK = false>
-__device__ __forceinline__ int cta_row_argmax(const char* row, int64_t nvec, u64* red, int* redc, u64 ref = 0,
-                                              int* rank = nullptr) {
+__device__ __forceinline__ int cta_row_argmax(const char* row, int64_t nvec, u64* red, int* redc, float xp = 0.f,
+                                              int prop = -1, int* rank = nullptr) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int c = 0;
-  u64 k = thread_row_best<T, VECTOR, RANK>(row, tid, nvec, BPD_NT, ref, &c);
+  u64 k = thread_row_best<T, VECTOR, RANK>(row, tid, nvec, BPD_NT, xp, prop, &c);
   k = warp_max_u64(k);
   if constexpr (RANK) c = __reduce_add_sync(FULL, c);
   if (lane == 0) {
@@ -130,8 +137,8 @@ __global__ void __launch_bounds__(BPD_NT) bpd_verify_kernel(const void* logits, 
   for (int p = 0; p < k - 1; ++p) {
     const int prop = __ldg(props + p + 1);
     int rank = 0;
-    const u64 ref = RANK ? token_key<T>(row_ptr(p, 0), prop, V) : 0ull;
-    const int am = cta_row_argmax<T, VECTOR, RANK>(row_ptr(p, 0), nvec, red, redc, ref, &rank);
+    const float xp = RANK ? token_value<T>(row_ptr(p, 0), prop, V) : 0.f;
+    const int am = cta_row_argmax<T, VECTOR, RANK>(row_ptr(p, 0), nvec, red, redc, xp, prop, &rank);
     if (tid == 0) am_p[p] = am;
     last_p = p;
     if (!bpd_passes(crit, prop, am, rank, V)) break;
@@ -184,14 +191,29 @@ struct RowStage {
   u32 phase;
 };
 
-// The row's argmax; with RANK also *rank = the number of keys above `ref`.
+__device__ __forceinline__ u32 gt_bf16x2(u32 a, u32 b) {
+  u32 d;
+  asm("set.gt.u32.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ u32 eq_bf16x2(u32 a, u32 b) {
+  u32 d;
+  asm("set.eq.u32.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// The row's argmax; with RANK also *rank = the number of elements that beat proposal
+// `prop` (a larger logit, or an equal one at a lower id).  bf16 vectors count with packed
+// compares (each true half of the mask is 16 set bits); an equal element sends the vector
+// through the per-element test.
 template <typename T, bool VECTOR, bool RANK = false>
 __device__ int row_argmax(const char* row, int V, RowStage& st, u64* red, int* status, int* redc = nullptr,
-                          u64 ref = 0, int* rank = nullptr) {
+                          int prop = -1, int* rank = nullptr) {
   constexpr int VEC = VECTOR ? Vec16<T>::N : 1;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   u64 best = 0;
   int cnt = 0;
+  float xp = 0.f;
   if constexpr (VECTOR) {
     // the row in chunks of at most BPD_BUF bytes: one bulk copy each, then a scan of the
     // staged vectors from shared memory
@@ -207,6 +229,7 @@ __device__ int row_argmax(const char* row, int V, RowStage& st, u64* red, int* s
         mbar_expect_tx(st.bar, static_cast<u32>(nv) * 16u);
         bulk_g2s(st.buf, row + static_cast<int64_t>(c0) * 16, static_cast<u32>(nv) * 16u, st.bar);
       }
+      if (RANK && c0 == 0) xp = token_value<T>(row, prop, V);   // in flight with the copy
       if (!mbar_wait(st.bar, st.phase)) set_status(status, VBS_ETIMEOUT);
       st.phase ^= 1u;
       const uint4* v = reinterpret_cast<const uint4*>(st.buf);
@@ -215,10 +238,23 @@ __device__ int row_argmax(const char* row, int V, RowStage& st, u64* red, int* s
         const float m = VecMax<T>::finish(VecMax<T>::fold(q, VecMax<T>::NEG));
         if (m > bv || bi < 0) { bv = m; bi = c0 + i; bq = q; }
         if constexpr (RANK) {
-          float x[VEC];
-          Vec16<T>::unpack(q, x);
+          const int v0 = (c0 + i) * VEC;
+          bool tie = true;
+          if constexpr (Elem<T>::BYTES == 2) {
+            const u32 xb = __float_as_uint(xp) >> 16, refw = xb | (xb << 16);
+            cnt += static_cast<int>((__popc(gt_bf16x2(q.x, refw)) + __popc(gt_bf16x2(q.y, refw)) +
+                                     __popc(gt_bf16x2(q.z, refw)) + __popc(gt_bf16x2(q.w, refw))) >> 4);
+            tie = (eq_bf16x2(q.x, refw) | eq_bf16x2(q.y, refw) | eq_bf16x2(q.z, refw) | eq_bf16x2(q.w, refw)) != 0u;
+          }
+          if (tie) {
+            float x[VEC];
+            Vec16<T>::unpack(q, x);
 #pragma unroll
-          for (int e2 = 0; e2 < VEC; ++e2) cnt += make_key(x[e2], static_cast<u32>((c0 + i) * VEC + e2)) > ref ? 1 : 0;
+            for (int e2 = 0; e2 < VEC; ++e2) {
+              if constexpr (Elem<T>::BYTES == 2) cnt += (x[e2] == xp && v0 + e2 < prop) ? 1 : 0;
+              else cnt += beats(x[e2], v0 + e2, xp, prop);
+            }
+          }
         }
       }
     }
@@ -231,10 +267,12 @@ __device__ int row_argmax(const char* row, int V, RowStage& st, u64* red, int* s
       best = make_key(bv, static_cast<u32>(bi * VEC + e));
     }
   } else {
+    if constexpr (RANK) xp = token_value<T>(row, prop, V);
     for (int i = tid; i < V; i += BPD_RT) {
-      const u64 k = make_key(Elem<T>::load(row, i), static_cast<u32>(i));
+      const float x = Elem<T>::load(row, i);
+      const u64 k = make_key(x, static_cast<u32>(i));
       best = k > best ? k : best;
-      if constexpr (RANK) cnt += k > ref ? 1 : 0;
+      if constexpr (RANK) cnt += beats(x, i, xp, prop);
     }
   }
   best = warp_max_u64(best);
@@ -302,7 +340,6 @@ __global__ void __launch_bounds__(BPD_RT, 3) bpd_verify_queue_kernel(const void*
   extern __shared__ __align__(128) unsigned char bpd_smem[];
   __shared__ u64 red[BPD_RT / 32 + 1];
   __shared__ int redc[BPD_RT / 32 + 1];
-  __shared__ u64 s_ref;
   __shared__ __align__(8) u64 bar;
   __shared__ int s_unit, s_b, s_h, s_q;
   const int tid = threadIdx.x;
@@ -337,9 +374,7 @@ __global__ void __launch_bounds__(BPD_RT, 3) bpd_verify_queue_kernel(const void*
       const int prop = __ldg(props + p + 1);
       int rank = 0;
       if constexpr (RANK) {
-        if (tid == 0) s_ref = token_key<T>(row, prop, V);
-        __syncthreads();
-        am = row_argmax<T, VECTOR, true>(row, V, st, red, status, redc, s_ref, &rank);
+        am = row_argmax<T, VECTOR, true>(row, V, st, red, status, redc, prop, &rank);
       } else {
         am = row_argmax<T, VECTOR>(row, V, st, red, status);
       }
