@@ -135,6 +135,31 @@ int bs_step(vbs_bs* ctx, const void* logits, int64_t ld, float* scores, int32_t*
  */
 int bs_step_two_pass(vbs_bs* ctx, const void* logits, int64_t ld, float* scores, int32_t* seqs, int32_t* beam_idx,
                      int32_t* tokens, int32_t* all_done);
+/*
+ * Vocabulary shards (the row's logits split by column, e.g. across the ranks of
+ * a vocabulary-parallel LM head): each shard reduces every row to a partial
+ * (the shard's max, scaled sum of exponentials and its K = 2W best (logit,
+ * token) keys, token ids global), the partials of all shards are exchanged
+ * (the caller's job: one all-gather of bs_shard_partial_bytes() bytes per
+ * shard), and one merge finishes the step exactly as bs_step would on the
+ * whole rows (the row LSE is the log-sum-exp of the shards', the row's best 2W
+ * come from the shards' lists).
+ *   bs_shard_partial_bytes: the size of one shard's partial buffer.
+ *   bs_step_shard: columns [v0, v0 + Vs) of the step's logits, logits_shard[R,
+ *     ld] (device, row stride ld >= Vs), with the step's current scores (read
+ *     only: rows of finished sentences and -inf scores are skipped); writes the
+ *     partial to `partial` (device, 16-byte aligned).  Does not advance the step.
+ *   bs_step_merge_shards: n_shards partials, contiguous ([n_shards][bytes],
+ *     device), whose shards tile [0, V) (not checked); then as bs_step.
+ *     n_shards <= min(256 / 2W, 128 / W) (VBS_EINVAL beyond).
+ * The pages' vocabulary-parallel reading: the step reduces per row over V, so
+ * per-shard (max, sum, top-2W) combine exactly; no pages' counterpart as calls.
+ */
+int bs_shard_partial_bytes(vbs_bs* ctx, int64_t* bytes);
+int bs_step_shard(vbs_bs* ctx, const void* logits_shard, int64_t ld, int v0, int Vs, const float* scores,
+                  void* partial);
+int bs_step_merge_shards(vbs_bs* ctx, int n_shards, const void* partials, float* scores, int32_t* seqs,
+                         int32_t* beam_idx, int32_t* tokens, int32_t* all_done);
 
 /*
  * Final choice ([BS] after the loop): the live beams of every sentence not yet

@@ -180,9 +180,12 @@ def compare_finished(case, tr: OracleTrace, fin: dict, t: int):
                 assert ns[r] == hy.ns
 
 
-def run_gpu_case(case: BeamCase, tr: OracleTrace, device="cuda", check_every_step=True, two_pass=False):
+def run_gpu_case(case: BeamCase, tr: OracleTrace, device="cuda", check_every_step=True, two_pass=False,
+                 shards=None):
     """Run the CUDA path over the oracle's steps and compare everything; returns the BeamSearch.
-    With two_pass, every step goes through the two-pass coarse-selection ablation."""
+    With two_pass, every step goes through the two-pass coarse-selection ablation; with
+    shards (a list of column boundaries 0 < c1 < ... < V), through per-shard partials and
+    their merge."""
     import verify_bs_step_gb300 as vbs
 
     bias_dev = synth.zipf_bias(case.V, case.seed, device) if case.kind == "llama" else None
@@ -193,7 +196,12 @@ def run_gpu_case(case: BeamCase, tr: OracleTrace, device="cuda", check_every_ste
     for t in range(1, len(tr.steps) + 1):
         logits = step_logits(case, t, tr.salts[t - 1], device, bias_dev, bias_cpu)
         lg = logits[:, :case.V] if case.ld_pad else logits
-        bi, tok, sc = bs.step_two_pass(lg) if two_pass else bs.step(lg)
+        if shards:
+            cuts = [0] + list(shards) + [case.V]
+            parts = [bs.shard_partial(lg[:, c0:c1], c0) for c0, c1 in zip(cuts[:-1], cuts[1:])]
+            bi, tok, sc = bs.merge_shards(torch.stack(parts))
+        else:
+            bi, tok, sc = bs.step_two_pass(lg) if two_pass else bs.step(lg)
         if check_every_step or t == len(tr.steps):
             torch.cuda.synchronize()
             compare_step(case, tr, t, bi.cpu().numpy(), tok.cpu().numpy(), sc.cpu().numpy(),

@@ -284,3 +284,42 @@ def test_two_pass_ablation_llama_shape():
     tr = hz.run_oracle(case)
     bs = hz.run_gpu_case(case, tr, two_pass=True)
     bs.close()
+
+
+# ------------------------------------------------------------------------------------
+# vocabulary shards: per-shard partials merged into the step (bs_step_shard / _merge_shards)
+# ------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("kind,B,W,V,T,dtype,eos,shards", [
+    ("tiny", 3, 2, 6, 8, torch.float32, 5, [3]),
+    ("sweep", 8, 4, 32000, 16, torch.bfloat16, 7, [10000]),
+    ("sweep", 6, 4, 32000, 12, torch.bfloat16, 3, [7, 12345, 20001]),      # unaligned shards: element path
+    ("sweep", 3, 16, 4096, 10, torch.float32, 11, [512, 1024, 2048, 3000]),  # K = 32
+    ("sweep", 4, 3, 1003, 12, torch.float32, 2, [501]),
+])
+def test_vocab_shards_match_oracle(kind, B, W, V, T, dtype, eos, shards):
+    case = hz.BeamCase(kind, B, W, V, T, dtype, eos=eos, alpha=0.6, seed=B * 17 + V % 103)
+    tr = hz.run_oracle(case)
+    bs = hz.run_gpu_case(case, tr, shards=shards)
+    hz.compare_finalize(case, tr, bs)
+    bs.close()
+
+
+def test_vocab_shards_llama_shape():
+    case = hz.BeamCase("llama", 64, 4, 128256, 2, torch.bfloat16, eos=2, alpha=0.6, seed=1236, checked=[3, 40])
+    tr = hz.run_oracle(case)
+    bs = hz.run_gpu_case(case, tr, shards=[32064, 64128, 96192])   # four shards of a 4-way vocab-parallel head
+    bs.close()
+
+
+def test_vocab_shards_limits():
+    import verify_bs_step_gb300 as vbs
+    bs = vbs.BeamSearch(2, 4, 64, eos=3, max_len=4, dtype=torch.float32)
+    lg = torch.zeros(8, 64, device="cuda")
+    with pytest.raises(vbs.VbsError):
+        bs.shard_partial(lg[:, 60:64 + 0], 61)             # past V
+    part = bs.shard_partial(lg, 0)
+    with pytest.raises(vbs.VbsError) as e:
+        bs.merge_shards(part.unsqueeze(0).repeat(33, 1))    # more shards than the merge holds (W 4: 32)
+    assert e.value.status == vbs.EINVAL
+    bs.close()

@@ -63,3 +63,39 @@ def test_single_process_defaults(monkeypatch):
         monkeypatch.delenv(k, raising=False)
     assert bench.dist_env() == (0, 0, 1)
     assert bench.max_over_ranks(2.0, 1) == 2.0 and bench.sum_over_ranks(5, 1) == 5
+
+
+def _gather_worker(rank, world, port, out):
+    import torch
+    import torch.distributed as dist
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        import verify_bs_step_gb300 as vbs
+        part = torch.full((40,), rank + 1, dtype=torch.uint8)
+        part[0] = 200 + rank
+        got = vbs.gather_shard_partials(part)
+        out[rank] = got.tolist()
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+def test_vocab_shard_partials_gather_in_rank_order():
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as mgr:
+        out = mgr.dict()
+        port = _free_port()
+        procs = [ctx.Process(target=_gather_worker, args=(r, 2, port, out)) for r in range(2)]
+        for p in procs:
+            p.start()
+        for p in procs:
+            p.join(120)
+            assert p.exitcode == 0
+        res = dict(out)
+    for r in (0, 1):
+        rows = res[r]
+        assert len(rows) == 2
+        for k in (0, 1):
+            assert rows[k][0] == 200 + k and rows[k][1:] == [k + 1] * 39

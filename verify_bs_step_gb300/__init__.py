@@ -15,7 +15,7 @@ import torch
 
 __all__ = ["BeamSearch", "PagedKV", "kv_reorder", "bpd_propose", "bpd_verify", "VbsError", "lib",
            "LP_GNMT", "LP_POWER", "ES_FALSE", "ES_TRUE", "ES_NEVER", "F32", "BF16", "BPD_EXACT", "BPD_TOPK",
-           "BPD_DISTANCE"]
+           "BPD_DISTANCE", "gather_shard_partials"]
 
 F32, BF16 = 0, 1
 LP_GNMT, LP_POWER = 0, 1
@@ -51,6 +51,9 @@ SIGNATURES = {
     "kv_paged_prepare": (_c_int, [_vp, _c_int]),
     "kv_paged_reorder": (_c_int, [_vp, _vp, _c_int]),
     "bs_step_two_pass": (_c_int, [_vp, _vp, _c_i64, _vp, _vp, _vp, _vp, _vp]),
+    "bs_shard_partial_bytes": (_c_int, [_vp, _vp]),
+    "bs_step_shard": (_c_int, [_vp, _vp, _c_i64, _c_int, _c_int, _vp, _vp]),
+    "bs_step_merge_shards": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _vp, _vp, _vp]),
     "bs_step_paged": (_c_int, [_vp, _vp, _c_i64, _vp, _vp, _vp, _vp, _vp, _vp, _c_int]),
     "kv_paged_copy": (_c_int, [_vp]),
     "kv_paged_table": (_c_int, [_vp, _pp, ctypes.POINTER(_c_int)]),
@@ -169,6 +172,32 @@ class BeamSearch:
                                       _vp(self.scores.data_ptr()), _vp(self.seqs.data_ptr()),
                                       _vp(self.beam_idx.data_ptr()), _vp(self.tokens.data_ptr()),
                                       _vp(self.all_done.data_ptr())), "bs_step_two_pass")
+        return self.beam_idx, self.tokens, self.scores
+
+    def shard_partial(self, logits_shard: torch.Tensor, v0: int) -> torch.Tensor:
+        """The partial of vocabulary columns [v0, v0 + Vs) of this step's logits (a [R, Vs] view,
+        unit stride along V): a uint8 device tensor of bs_shard_partial_bytes()."""
+        if logits_shard.dim() != 2 or logits_shard.shape[0] != self.R or logits_shard.stride(1) != 1:
+            raise ValueError(f"logits_shard must be [{self.R}, Vs] with unit stride along V")
+        if logits_shard.dtype != self.dtype:
+            raise ValueError(f"logits must be {self.dtype}")
+        n = ctypes.c_int64()
+        _check(lib().bs_shard_partial_bytes(self.ctx, ctypes.byref(n)), "bs_shard_partial_bytes")
+        out = torch.empty(n.value, dtype=torch.uint8, device=self.device)
+        _check(lib().bs_step_shard(self.ctx, _dev_ptr(logits_shard, "logits"), logits_shard.stride(0), v0,
+                                   logits_shard.shape[1], _vp(self.scores.data_ptr()), _vp(out.data_ptr())),
+               "bs_step_shard")
+        return out
+
+    def merge_shards(self, partials: torch.Tensor):
+        """Finish the step from the shards' partials ([n_shards, bytes] uint8, contiguous, device);
+        returns (beam_idx, tokens, scores) views like step()."""
+        if partials.dim() != 2 or not partials.is_contiguous() or partials.dtype != torch.uint8:
+            raise ValueError("partials must be a contiguous [n_shards, bytes] uint8 tensor")
+        _check(lib().bs_step_merge_shards(self.ctx, partials.shape[0], _dev_ptr(partials, "partials"),
+                                          _vp(self.scores.data_ptr()), _vp(self.seqs.data_ptr()),
+                                          _vp(self.beam_idx.data_ptr()), _vp(self.tokens.data_ptr()),
+                                          _vp(self.all_done.data_ptr())), "bs_step_merge_shards")
         return self.beam_idx, self.tokens, self.scores
 
     def step_paged(self, logits: torch.Tensor, kv: "PagedKV", t_valid: int):
@@ -406,3 +435,17 @@ def bpd_verify(logits: torch.Tensor, proposals: torch.Tensor, eos: int = -1, kha
                                        _dev_ptr(khat, "khat", torch.int32), _dev_ptr(next_out, "next", torch.int32),
                                        _stream(logits.device)), "bpd_verify_approx")
     return khat, next_out
+
+
+def gather_shard_partials(partial: torch.Tensor, group=None) -> torch.Tensor:
+    """All-gather one shard partial per rank (torch.distributed, rank order): [world, bytes].
+
+    Each rank of a vocabulary-parallel LM head holds the columns of one shard; after
+    BeamSearch.shard_partial this exchange gives every rank the partials that
+    BeamSearch.merge_shards takes.
+    """
+    import torch.distributed as dist
+    world = dist.get_world_size(group)
+    out = torch.empty(world, partial.numel(), dtype=partial.dtype, device=partial.device)
+    dist.all_gather(list(out.unbind(0)), partial.contiguous(), group=group)
+    return out

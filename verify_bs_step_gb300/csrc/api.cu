@@ -1,6 +1,7 @@
 // The C ABI of libvbs: argument checks, context lifetime, workspace layout and
 // kernel launches.  No entry point after an init allocates device memory.
 
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
@@ -151,8 +152,14 @@ VBS_EXPORT int bs_init(vbs_bs** out, int batch, int W, int V, int eos, double al
     }
   }
 
+  // vocabulary-shard merges: as many shards per row as the merge kernel's partial buffer holds
+  a.shard_max = std::min(vbs::PART_KEYS / a.K, vbs::PART_KEYS / 2 / W);
   Carver cv;
   for (int pass = 0; pass < 2; ++pass) {
+    a.shard_M = cv.take<float>(R * a.shard_max);
+    a.shard_l = cv.take<float>(R * a.shard_max);
+    a.shard_key = cv.take<u64>(R * a.shard_max * a.K);
+    a.row_ns = cv.take<int>(R);
     a.part_M = cv.take<float>(R * a.P);
     a.part_l = cv.take<float>(R * a.P);
     a.part_key = cv.take<u64>(R * a.P * a.K);
@@ -268,6 +275,47 @@ VBS_EXPORT int bs_step_two_pass(vbs_bs* c, const void* logits, int64_t ld, float
   int st = step_args(c, logits, ld, scores, seqs, beam_idx, tokens, all_done, a, vec_ok);
   if (st != VBS_OK) return st;
   st = vbs::launch_bs_step_two_pass(a, vec_ok, c->stream);
+  if (st != VBS_OK) return st;
+  c->step += 1;
+  return VBS_OK;
+}
+
+VBS_EXPORT int bs_shard_partial_bytes(vbs_bs* c, int64_t* bytes) {
+  if (!c || !bytes) return VBS_EINVAL;
+  size_t off_l, off_key, b;
+  vbs::shard_partial_layout(c->a.R, c->a.K, &off_l, &off_key, &b);
+  *bytes = static_cast<int64_t>(b);
+  return VBS_OK;
+}
+
+VBS_EXPORT int bs_step_shard(vbs_bs* c, const void* logits_shard, int64_t ld, int v0, int Vs, const float* scores,
+                             void* partial) {
+  if (!c || !logits_shard || !scores || !partial) return VBS_EINVAL;
+  if (v0 < 0 || Vs < 1 || static_cast<int64_t>(v0) + Vs > c->a.V || ld < Vs) return VBS_EINVAL;
+  if (!c->reset_done || c->step >= c->a.max_len) return VBS_ESTATE;
+  if (!aligned16(partial)) return VBS_EALIGN;
+  vbs::BsArgs a = c->a;
+  a.logits = logits_shard;
+  a.ld = ld;
+  a.V = Vs;
+  a.vbase = v0;
+  a.scores = const_cast<float*>(scores);
+  const int es = a.dtype == VBS_BF16 ? 2 : 4;
+  const int VEC = 16 / es;
+  const bool vec_ok = aligned16(logits_shard) && (ld * es) % 16 == 0 && Vs % VEC == 0;
+  return vbs::launch_bs_shard_partial(a, vec_ok, partial, c->stream);
+}
+
+VBS_EXPORT int bs_step_merge_shards(vbs_bs* c, int n_shards, const void* partials, float* scores, int32_t* seqs,
+                                    int32_t* beam_idx, int32_t* tokens, int32_t* all_done) {
+  if (!partials) return VBS_EINVAL;
+  vbs::BsArgs a;
+  bool vec_ok = false;
+  // the logits pointer is unused by the merge: the partials stand in for it
+  int st = step_args(c, partials, c ? c->a.V : 0, scores, seqs, beam_idx, tokens, all_done, a, vec_ok);
+  if (st != VBS_OK) return st;
+  if (n_shards < 1 || n_shards > a.shard_max) return VBS_EINVAL;
+  st = vbs::launch_bs_merge_shards(a, n_shards, partials, c->stream);
   if (st != VBS_OK) return st;
   c->step += 1;
   return VBS_OK;

@@ -54,6 +54,13 @@ struct BsArgs {
   unsigned long long* part_key;
   unsigned* rtopk_bar;            // [R] the two-pass ablation's per-row bar (ordered logit bits)
   int* row_one;                   // [R] all 1: the two-pass ablation writes one partial slot per row
+  int vbase;                      // token id of the first logit column (a vocabulary shard's offset)
+  // vocabulary shards: up to shard_max partials per row, merged by the merge kernel
+  int shard_max;
+  float* shard_M;                 // [R][shard_max]
+  float* shard_l;
+  unsigned long long* shard_key;  // [R][shard_max][K]
+  int* row_ns;                    // [R] the number of shards of the current merge
   int* row_p0;                    // [R] the first CTA whose range holds row r
   int* row_np;                    // [R] the number of CTAs (partials) holding row r
   int* done_count;                // sentences finished (step-local counter)
@@ -77,6 +84,11 @@ struct BsArgs {
 int launch_bs_step(const BsArgs& a, int grid, bool vector_ok, cudaStream_t s);
 bool bs_can_fuse_remap(const BsArgs& a, const PagedArgs& kv);
 int launch_bs_step_two_pass(const BsArgs& a, bool vector_ok, cudaStream_t s);
+// one vocabulary shard's per-row partial (max, scaled sum, K best keys) into a caller buffer laid
+// out as shard_partial_layout gives, and the merge of n such buffers
+void shard_partial_layout(int R, int K, size_t* off_l, size_t* off_key, size_t* bytes);
+int launch_bs_shard_partial(const BsArgs& a, bool vector_ok, void* partial, cudaStream_t s);
+int launch_bs_merge_shards(const BsArgs& a, int n_shards, const void* partials, cudaStream_t s);
 int launch_bs_reset(const BsArgs& a, cudaStream_t s);
 int launch_bs_finalize(const BsArgs& a, const float* scores, const int32_t* seqs, int n_ret, int32_t* out_seqs,
                        int32_t* out_len, float* out_score, cudaStream_t s);

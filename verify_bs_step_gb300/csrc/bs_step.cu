@@ -1575,7 +1575,7 @@ __global__ void __launch_bounds__(RT_NT) rtopk_pass2_kernel(const BsArgs a) {
         if (i >= n) continue;
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
-          const u64 key = make_key(x[u][e], static_cast<u32>(i * VEC + e));
+          const u64 key = make_key(x[u][e], static_cast<u32>(a.vbase + i * VEC + e));
           if (key >= b) {
             const int pos = atomicAdd(&cnt, 1);
             if (pos < RT_CAP) q[pos] = key;
@@ -1620,6 +1620,79 @@ int launch_bs_step_two_pass(const BsArgs& a0, bool vector_ok, cudaStream_t s) {
     }
   }
   if (cudaGetLastError() != cudaSuccess) return VBS_ECUDA;
+  return launch_merge(a, s);
+}
+
+// ---------------------------------------------------------------------------------------
+// vocabulary shards: each shard's rows reduce to a partial with the two passes above (token
+// ids offset by the shard's first column), and the merge kernel combines the shards'
+// partials as it combines the stream kernel's, with the shards as a row's partial slots
+// ---------------------------------------------------------------------------------------
+
+void shard_partial_layout(int R, int K, size_t* off_l, size_t* off_key, size_t* bytes) {
+  const size_t a = (static_cast<size_t>(R) * 4 + 15) / 16 * 16;
+  *off_l = a;
+  *off_key = 2 * a;
+  *bytes = 2 * a + static_cast<size_t>(R) * K * 8;
+}
+
+int launch_bs_shard_partial(const BsArgs& a0, bool vector_ok, void* partial, cudaStream_t s) {
+  size_t off_l, off_key, bytes;
+  shard_partial_layout(a0.R, a0.K, &off_l, &off_key, &bytes);
+  BsArgs a = a0;
+  a.P = 1;                                          // one slot per row, in the caller's buffer
+  a.part_M = static_cast<float*>(partial);
+  a.part_l = reinterpret_cast<float*>(static_cast<char*>(partial) + off_l);
+  a.part_key = reinterpret_cast<u64*>(static_cast<char*>(partial) + off_key);
+  if (a.dtype == VBS_BF16) {
+    if (vector_ok) {
+      rtopk_pass1_kernel<bf16_t, true><<<a.R, RT_NT, 0, s>>>(a);
+      rtopk_pass2_kernel<bf16_t, true><<<a.R, RT_NT, 0, s>>>(a);
+    } else {
+      rtopk_pass1_kernel<bf16_t, false><<<a.R, RT_NT, 0, s>>>(a);
+      rtopk_pass2_kernel<bf16_t, false><<<a.R, RT_NT, 0, s>>>(a);
+    }
+  } else {
+    if (vector_ok) {
+      rtopk_pass1_kernel<float, true><<<a.R, RT_NT, 0, s>>>(a);
+      rtopk_pass2_kernel<float, true><<<a.R, RT_NT, 0, s>>>(a);
+    } else {
+      rtopk_pass1_kernel<float, false><<<a.R, RT_NT, 0, s>>>(a);
+      rtopk_pass2_kernel<float, false><<<a.R, RT_NT, 0, s>>>(a);
+    }
+  }
+  return cudaGetLastError() == cudaSuccess ? VBS_OK : VBS_ECUDA;
+}
+
+// One warp per row: shard j's partial of row r goes to slot r * n + j.
+__global__ void bs_shard_scatter_kernel(const BsArgs a, int n, const char* partials, size_t off_l, size_t off_key,
+                                        size_t bytes) {
+  const int r = blockIdx.x, lane = threadIdx.x;
+  const int K = a.K;
+  for (int j = 0; j < n; ++j) {
+    const char* p = partials + static_cast<size_t>(j) * bytes;
+    const int64_t slot = static_cast<int64_t>(r) * n + j;
+    if (lane == 0) {
+      a.shard_M[slot] = reinterpret_cast<const float*>(p)[r];
+      a.shard_l[slot] = reinterpret_cast<const float*>(p + off_l)[r];
+    }
+    if (lane < K) a.shard_key[slot * K + lane] = reinterpret_cast<const u64*>(p + off_key)[static_cast<int64_t>(r) * K + lane];
+  }
+  if (lane == 0) a.row_ns[r] = n;
+}
+
+int launch_bs_merge_shards(const BsArgs& a0, int n_shards, const void* partials, cudaStream_t s) {
+  size_t off_l, off_key, bytes;
+  shard_partial_layout(a0.R, a0.K, &off_l, &off_key, &bytes);
+  bs_shard_scatter_kernel<<<a0.R, 32, 0, s>>>(a0, n_shards, static_cast<const char*>(partials), off_l, off_key,
+                                               bytes);
+  if (cudaGetLastError() != cudaSuccess) return VBS_ECUDA;
+  BsArgs a = a0;
+  a.P = n_shards;
+  a.part_M = a.shard_M;
+  a.part_l = a.shard_l;
+  a.part_key = a.shard_key;
+  a.row_np = a.row_ns;
   return launch_merge(a, s);
 }
 
