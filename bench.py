@@ -652,12 +652,15 @@ def run_profile(kernel: str):
     _build.build()
     dev = torch.device("cuda", 0)
     wl = WORKLOAD
-    if kernel == "bs_step":
+    if kernel in ("bs_step", "bs_step_two_pass"):
         B, W, V, T = wl["B"], wl["W"], wl["V"], wl["T"]
         ring = make_logits_ring(torch, synth, 3, wl["seed"], dev, B, W, V)
         bs = vbs.BeamSearch(B, W, V, eos=wl["eos"], alpha=wl["alpha"], max_len=T, dtype=torch.bfloat16, device=dev)
         for i in range(8):
-            bs.step(ring[i % 3])
+            if kernel == "bs_step":
+                bs.step(ring[i % 3])
+            else:
+                bs.step_two_pass(ring[i % 3])
         bs.close()
     elif kernel == "bpd_verify":
         B, k, V = 256, 8, 32000
