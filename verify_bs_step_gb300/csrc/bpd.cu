@@ -6,13 +6,18 @@
 // every proposal up to khat equals the base model's argmax given the proposals
 // before it; khat >= 1; accept) and §4 (the combined scoring and proposal model:
 // the verify call also yields the next iteration's proposals from position
-// khat).  Layout: logits[b, p, h, :] is head h+1 at proposal position p+1.
+// khat), and §5 (approximate inference: the top-k and distance tests and the
+// minimum block, whose formulas the pages' text lacks; the readings are stated at
+// bpd_verify_approx).  Layout: logits[b, p, h, :] is head h+1 at proposal
+// position p+1.
 //
-// One CTA per batch element.  The verify checks are sequential (each decides
-// whether the next row is needed), so only the rows the definition needs are
-// read: head 0 at positions 0..khat-1 (at most k-1 of them), then the k heads
-// at position khat-1, the already-known head 0 reused.  Argmax ties go to the
-// lower token id, through a (logit, token) key where a larger key is better.
+// The verify checks are sequential (each decides whether the next row is
+// needed), so only the rows the definition needs are read: head 0 at positions
+// 0..khat-1 (at most k-1 of them), then the k heads at position khat-1, the
+// already-known head 0 reused.  Batches up to 16384 run as a persistent work
+// queue (chains first, then the published head rows); larger ones one CTA per
+// batch element.  Argmax ties go to the lower token id, through a (logit, token)
+// key where a larger key is better.
 
 #include "common.cuh"
 #include "bs_internal.h"

@@ -1,26 +1,30 @@
-// Fused batched beam-search step (sm_103a): two kernels per step.
+// Fused batched beam-search step (sm_103a).
 //
-// bs_stream_kernel, one CTA per SM: the R = B*W logit rows are cut into G equal
-// ranges of the flattened [R, V] index space.  In each CTA a producer warp
-// streams the range through a 6-stage ring of 32 KiB shared-memory chunks with
-// bulk (TMA) copies completing on mbarriers, and 16 consumer warps read each
-// chunk once from shared memory: per 32-element tile a thread updates an
-// online log-sum-exp (log2 domain, SFU exp2) and compares the tile maximum
-// with a CTA-wide threshold key.  Only a lane whose tile can hold one of the
-// row's 2W best (logit, token) pairs leaves the streaming loop, to queue the
-// qualifying keys in a CTA-wide shared-memory queue.  The threshold is seeded
-// at the start of every row segment from the consumers' first-tile maxima and
-// is raised from the queue every 16 pushes; it never passes the segment's K-th
-// best, so an element below it is provably outside the row's top K.  A row
-// segment ends in one partial (max, scaled sum, K sorted keys).
+// The streaming part, shared by both launch shapes: a producer warp streams logit rows
+// through a 6-stage ring of 32 KiB shared-memory chunks with bulk (TMA) copies completing
+// on mbarriers, and 16 consumer warps read each chunk once: per 32-element tile a thread
+// updates an online log-sum-exp (log2 domain, SFU exp2) and compares the tile maximum with
+// its row's threshold.  The threshold only takes values that bound the row's K-th best
+// logit from below: at a row's first chunk the consumer warps each seed it with the K-th
+// best of their lane maxima and meet at a named barrier; a tile whose maximum reaches it
+// queues one entry (maximum, column, and a bound on its second-largest value with the
+// maximum's place), and one warp per chunk raises it from the queue.  At the end of the
+// row the K-th best queued maximum is the final bar; a tile at the bar gives its key from
+// its queue entry when its runner-up bound is below the bar, otherwise it is read again.
+// A queue overflow falls back to rescanning the row.
 //
-// bs_merge_kernel, one CTA per sentence, launched as a programmatic dependent
-// of the stream kernel (it starts as the stream CTAs retire and waits for
-// their writes): each row's LSE and top-K from its partials, the sentence's
-// best 2W candidates by (score desc, flat index asc) found by ranking, the
-// walk that moves EOS hits into the finished set, the stopping test, the
-// outputs and the in-place sequence gather.  No CTA waits on another CTA of
-// its own grid; every mbarrier wait is bounded.
+// bs_cluster_kernel (one launch per step): one thread-block cluster per sentence, each CTA
+// streaming whole rows; the sentence's rows meet in distributed shared memory and one warp
+// merges them: row LSEs, the best 2W candidates by (score desc, flat index asc), the walk
+// that moves EOS hits into the finished set, the stopping test, the outputs and the
+// in-place sequence gather.  An instance with FUSE also runs the sentence's paged KV remap.
+//
+// bs_stream_kernel + bs_merge_kernel (shapes the cluster does not fit): one CTA per SM over
+// equal ranges of the flattened [R, V] space, each row segment ending in a partial (max,
+// scaled sum, K sorted keys), then one merge CTA per sentence, launched as a programmatic
+// dependent.  The same merge finishes the two-pass ablation and the vocabulary-shard path.
+//
+// No CTA waits on another CTA outside its cluster; every mbarrier wait is bounded.
 //
 // What is computed follows "Transformers中的Beam Search高效实现" (section
 // 多个样本同时进行beam search: log_softmax, add beam_scores, view [batch, W*V],

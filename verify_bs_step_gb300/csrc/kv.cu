@@ -7,14 +7,17 @@
 // entries and copies only when a shared block is written) and §9.2.4 (prompt
 // sharing).
 //
-// Both copy paths are pure byte movement, so they run on the bulk-copy (TMA)
+// The naive gather moves long contiguous runs, so it runs on the bulk-copy (TMA)
 // engine: one elected thread per CTA keeps a ring of shared-memory stages full
 // with cp.async.bulk global->shared loads (completing on mbarriers) and drains
-// them with cp.async.bulk shared->global stores (bulk groups).  The remap of
-// the paged table is sentence-local (blocks are never shared across
-// sentences), so it runs one CTA per sentence on shared-memory copies of the
-// sentence's table rows, reference counts and free stack, with one global
-// atomic per sentence and a deterministic allocation order (kv_remap.cuh).
+// them with cp.async.bulk shared->global stores (bulk groups).  The paged
+// copy-on-write moves short scattered runs, warp per run with 16-byte vectors.
+// The remap of the paged table is sentence-local (blocks are never shared
+// across sentences), so it runs one CTA per sentence on shared-memory copies of
+// the sentence's table rows, reference counts and free stack, with a
+// deterministic allocation order; each sentence writes its copy-on-write tasks
+// to its own task slots (kv_remap.cuh).  Both paged kernels are programmatic
+// dependents of their predecessor in the stream.
 
 #include "common.cuh"
 #include "bs_internal.h"
