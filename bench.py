@@ -586,6 +586,76 @@ def run_extras(args, torch, vbs, synth, dev, stream, peak):
     return extra
 
 
+def run_sweep(only=None):
+    """bs_step alone over the sweep grid: batch {1, 32, 256} x W {1, 4, 16} x V {32000, 128256,
+    256000} x {fp32, bf16}, N(0, 2) logits with the EOS logit lifted above the row maximum on ~2 % of
+    rows, GNMT alpha 0.6, early_stopping False.  One JSON line per shape.
+
+    Each shape runs 50-step decodes (the first step of each, where only beam 0 is live, untimed)
+    until 200 steps are timed; every step reads a different logits buffer of a ring that spans
+    more than 4 x L2 (distinct batches up to 32 of them, then copies at other addresses)."""
+    import torch
+
+    import synth
+    import verify_bs_step_gb300 as vbs
+    from verify_bs_step_gb300 import _build
+
+    _build.build()
+    dev = torch.device("cuda", 0)
+    peak, peak_src = measured_peaks()
+    stream = torch.cuda.Stream(dev)
+    vp = ctypes.c_void_p
+    T, EOS = 50, 7
+    for V in (32000, 128256, 256000):
+        for B in (1, 32, 256):
+            for W in (1, 4, 16):
+                for dt, dname, esz in ((torch.float32, "f32", 4), (torch.bfloat16, "bf16", 2)):
+                    if only and (B, W, V, dname) not in only:
+                        continue
+                    R = B * W
+                    per = R * V * esz
+                    n = max(2, -(-4 * 129_000_000 // per) + 1)
+                    base = [synth.batch_logits("sweep", B, W, V, seed=2024 + i, step=i, eos=EOS, dtype=dt,
+                                               device=dev) for i in range(min(n, 32))]
+                    ring = [base[i] if i < len(base) else base[i % len(base)].clone() for i in range(n)]
+                    with torch.cuda.stream(stream):
+                        bs = vbs.BeamSearch(B, W, V, eos=EOS, alpha=0.6, early_stopping=vbs.ES_FALSE, max_len=T,
+                                            dtype=dt, device=dev)
+                        L_ = vbs.lib()
+                        a_ = [vp(bs.scores.data_ptr()), vp(bs.seqs.data_ptr()), vp(bs.beam_idx.data_ptr()),
+                              vp(bs.tokens.data_ptr()), vp(bs.all_done.data_ptr())]
+                        prs = [vp(x.data_ptr()) for x in ring]
+                        ts, i = [], 0
+                        while len(ts) < 210:
+                            L_.bs_reset(bs.ctx, a_[0], a_[1])
+                            L_.bs_step(bs.ctx, prs[i % n], V, *a_)
+                            i += 1
+                            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                                   for _ in range(T - 1)]
+                            torch.cuda.synchronize()
+                            torch.cuda._sleep(int(2e5) * (T - 1))
+                            for e_a, e_b in evs:
+                                e_a.record(stream)
+                                L_.bs_step(bs.ctx, prs[i % n], V, *a_)
+                                e_b.record(stream)
+                                i += 1
+                            torch.cuda.synchronize()
+                            ts.extend(e_a.elapsed_time(e_b) for e_a, e_b in evs)
+                        assert bs.status() == 0
+                        bs.close()
+                    ts = ts[10:]
+                    avg = statistics.fmean(ts)
+                    byts = per + R * 16
+                    gbs = byts / (avg / 1e3) / 1e9
+                    print(json.dumps({"sweep": {"B": B, "W": W, "V": V, "dtype": dname}, "avg_us": round(avg * 1e3, 3),
+                                      "median_us": round(statistics.median(ts) * 1e3, 3),
+                                      "steps_per_s": round(1e3 / avg, 1), "bytes": byts,
+                                      "achieved_gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+                                      "peak": f"{peak} GB/s ({peak_src})", "ring": n}), flush=True)
+                    del ring, base
+                    torch.cuda.empty_cache()
+
+
 # ------------------------------------------------------------------------------------
 # the oracle on the host cores (cpu_baseline and the reference arm)
 # ------------------------------------------------------------------------------------
@@ -631,13 +701,48 @@ def oracle_sample(seconds: float, seed: int = 1236, max_units: int | None = None
     return units, time.perf_counter() - t0
 
 
+def _oracle_worker(seconds, seed, start, out):
+    """One process of the all-core sample: its own sentence, timed after every worker is ready."""
+    os.environ["OMP_NUM_THREADS"] = "1"
+    import torch
+    torch.set_num_threads(1)
+    oracle_sample(0.0, seed=seed, max_units=1)          # imports and first-touch outside the timing
+    start.wait()
+    out.put(oracle_sample(seconds, seed=seed))
+
+
+def oracle_all_cores(seconds: float, n: int | None = None):
+    """The oracle over independent sentences, one spawned process per host core (sentences do not
+    interact, so the batch splits across processes).  Returns (sentence_steps, elapsed_s, cores)."""
+    import multiprocessing as mp
+    if n is None:
+        n = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    ctx = mp.get_context("spawn")
+    start, out = ctx.Barrier(n), ctx.Queue()
+    procs = [ctx.Process(target=_oracle_worker, args=(seconds, 1236 + 7919 * i, start, out)) for i in range(n)]
+    for p in procs:
+        p.start()
+    res = [out.get(timeout=600) for _ in procs]
+    for p in procs:
+        p.join(timeout=60)
+    return sum(u for u, _ in res), max(e for _, e in res), n
+
+
 def cpu_baseline(seconds: float):
     units, el = oracle_sample(seconds)
     B = WORKLOAD["B"]
-    return {"value": round(units / B / el, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{units} sentence-steps of the workload (one sentence's W rows: fp64 log-softmax, "
-                      f"top-2W walk, paged KV remap + copy-on-write on a full-size pool), scaled by 1/{B} "
-                      f"to full-batch beam-steps; {el:.1f} s on 1 host core"}
+    out = {"value": round(units / B / el, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+           "sample": f"{units} sentence-steps of the workload (one sentence's W rows: fp64 log-softmax, "
+                     f"top-2W walk, paged KV remap + copy-on-write on a full-size pool), scaled by 1/{B} "
+                     f"to full-batch beam-steps; {el:.1f} s on 1 host core"}
+    try:
+        ua, ea, n = oracle_all_cores(seconds)
+        out["all_cores"] = {"value": round(ua / B / ea, 4), "unit": UNIT, "cores": n,
+                            "sample": f"{ua} sentence-steps in {ea:.1f} s, {n} processes (one per core, "
+                                      f"one sentence each, 1 thread each)"}
+    except Exception as e:                               # the single-core figure stands on its own
+        out["all_cores"] = f"not measured: {type(e).__name__}: {e}"
+    return out
 
 
 def run_reference(args, rank, world):
@@ -720,9 +825,13 @@ def main(argv=None):
     ap.add_argument("--no-extras", action="store_true", help="skip the secondary lines")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle time budget for cpu_baseline")
     ap.add_argument("--profile", default=None, help="run a few launches of one kernel (for ncu) and exit")
+    ap.add_argument("--sweep", action="store_true", help="time bs_step alone over the sweep grid and exit")
     args = ap.parse_args(argv)
     if args.profile:
         run_profile(args.profile)
+        return
+    if args.sweep:
+        run_sweep()
         return
     rank, local_rank, world = dist_env()
     if world > 1:

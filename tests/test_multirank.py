@@ -99,3 +99,11 @@ def test_vocab_shard_partials_gather_in_rank_order():
         assert len(rows) == 2
         for k in (0, 1):
             assert rows[k][0] == 200 + k and rows[k][1:] == [k + 1] * 39
+
+
+def test_oracle_all_cores_sums_the_processes():
+    """The all-core cpu_baseline: spawned processes, each timing its own sentence after a
+    common start; the units add up and the time is the longest process's."""
+    import bench
+    units, el, n = bench.oracle_all_cores(0.3, n=2)
+    assert n == 2 and units >= 2 and el >= 0.3
