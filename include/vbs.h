@@ -65,7 +65,7 @@ enum { VBS_ES_FALSE = 0, VBS_ES_TRUE = 1, VBS_ES_NEVER = 2 };
 
 /* Name of a status code (static string, never NULL). */
 const char* vbs_strerror(int status);
-/* Library version, major * 10000 + minor * 100 + patch. */
+/* Library version, major * 10000 + minor * 100 + patch.  Never fails. */
 int vbs_version(void);
 
 /* =============================================================================
@@ -99,6 +99,7 @@ int bs_init(vbs_bs** ctx, int batch, int W, int V, int eos, double alpha, int ea
  * the finished sets, clears the done flags and the step counter.
  * seqs may be NULL: the context then keeps the sequences in its own buffer
  * (bs_seqs() returns it), and every later call must also pass NULL.
+ * Errors: VBS_EINVAL (NULL ctx or scores), VBS_ECUDA.
  */
 int bs_reset(vbs_bs* ctx, float* scores, int32_t* seqs);
 
@@ -132,6 +133,7 @@ int bs_step(vbs_bs* ctx, const void* logits, int64_t ld, float* scores, int32_t*
  * logit; K = 2W), a second pass reads the row again and keeps the K best keys
  * among the logits >= R, then the per-sentence merge of bs_step runs.  It reads
  * the logits twice; bs_step reads them once.
+ * Errors: those of bs_step.
  */
 int bs_step_two_pass(vbs_bs* ctx, const void* logits, int64_t ld, float* scores, int32_t* seqs, int32_t* beam_idx,
                      int32_t* tokens, int32_t* all_done);
@@ -152,6 +154,10 @@ int bs_step_two_pass(vbs_bs* ctx, const void* logits, int64_t ld, float* scores,
  *   bs_step_merge_shards: n_shards partials, contiguous ([n_shards][bytes],
  *     device), whose shards tile [0, V) (not checked); then as bs_step.
  *     n_shards <= min(256 / 2W, 128 / W) (VBS_EINVAL beyond).
+ * Errors: VBS_EINVAL (NULL pointers; v0 < 0, Vs < 1, v0 + Vs > V or ld < Vs;
+ *   n_shards out of range), VBS_EALIGN (partial not 16-byte aligned),
+ *   VBS_ESTATE (no bs_reset yet, max_len steps already run, or another seqs
+ *   buffer than bs_reset's), VBS_ECUDA.
  * The pages' vocabulary-parallel reading: the step reduces per row over V, so
  * per-shard (max, sum, top-2W) combine exactly; no pages' counterpart as calls.
  */
@@ -171,6 +177,8 @@ int bs_step_merge_shards(vbs_bs* ctx, int n_shards, const void* partials, float*
  * out_score[batch] the winner's normalised score.  scores/seqs are the
  * buffers of the last bs_step (seqs NULL if the context keeps them).  The
  * context is not changed: finalize may be called more than once.
+ * Errors: VBS_EINVAL (NULL pointers), VBS_ESTATE (no bs_reset yet, or another
+ *   seqs buffer than bs_reset's), VBS_ECUDA.
  */
 int bs_finalize(vbs_bs* ctx, const float* scores, const int32_t* seqs, int32_t* out_seqs, int32_t* out_len,
                 float* out_score);
@@ -180,7 +188,8 @@ int bs_finalize(vbs_bs* ctx, const float* scores, const int32_t* seqs, int32_t* 
  * them from a stable ascending sort, so equal scores go latest-inserted
  * first).  Sentence b's j-th best is row b * n_return + j of out_seqs
  * [batch * n_return, max_len+1], out_len and out_score.  bs_finalize is the
- * n_return = 1 case.  Errors: VBS_EINVAL for n_return outside 1..W.
+ * n_return = 1 case.  Errors: those of bs_finalize; VBS_EINVAL for n_return
+ * outside 1..W.
  */
 int bs_finalize_n(vbs_bs* ctx, const float* scores, const int32_t* seqs, int n_return, int32_t* out_seqs,
                   int32_t* out_len, float* out_score);
@@ -191,18 +200,21 @@ int bs_finalize_n(vbs_bs* ctx, const float* scores, const int32_t* seqs, int n_r
  * |y|; serial[batch*W] int32 insertion numbers (set order = ascending serial);
  * tokens[batch*W, max_len+1] int32 (the first len entries are BOS + tokens);
  * done[batch] int32.  Slots at or beyond count[b] are unused.  Any pointer may
- * be NULL to skip that array.
+ * be NULL to skip that array.  Errors: VBS_EINVAL (NULL ctx), VBS_ECUDA.
  */
 int bs_finished(vbs_bs* ctx, int32_t* count, double* ns, int32_t* len, int32_t* serial, int32_t* tokens,
                 int32_t* done);
 
-/* The context's own sequence buffer [R, max_len+1] (device), used when bs_reset got NULL. */
+/* The context's own sequence buffer [R, max_len+1] (device), used when bs_reset got NULL.
+   Errors: VBS_EINVAL (NULL arguments). */
 int bs_seqs(vbs_bs* ctx, int32_t** seqs);
-/* Steps run since bs_reset. */
+/* Steps run since bs_reset.  Errors: VBS_EINVAL (NULL arguments). */
 int bs_steps(vbs_bs* ctx, int* steps);
-/* Synchronise the context's stream and return (then clear) its device status word. */
+/* Synchronise the context's stream and return (then clear) its device status word:
+   VBS_OK or the first VBS_E* a kernel recorded.  VBS_EINVAL for NULL, VBS_ECUDA when
+   the synchronisation or the read fails. */
 int bs_status(vbs_bs* ctx);
-/* Free the context (synchronises its stream first). NULL is a no-op. */
+/* Free the context (synchronises its stream first). NULL is a no-op.  Returns VBS_OK. */
 int bs_destroy(vbs_bs* ctx);
 
 /*
@@ -275,6 +287,18 @@ int kv_reorder(const vbs_kv_desc* desc, const void* src, void* dst, const int32_
  */
 typedef struct vbs_pkv vbs_pkv;
 
+/*
+ * Create a paged cache for `batch` sentences of W rows over the caller's pool
+ * (device, [batch * blocks_per_sentence][L][2][H][block][D] of desc's
+ * elem_bytes): blocks_per_sentence blocks per sentence, `block` positions per
+ * block, max_blocks table entries per row.  Allocates the table, counts, free
+ * stacks, copy-task slots and the saved state once; later calls allocate
+ * nothing.  All work goes to `stream`.
+ * Errors: VBS_EINVAL (bad geometry, NULL pool, W outside 1..16, non-positive
+ *   sizes, or a per-sentence table too large for one CTA's shared memory:
+ *   W * max_blocks + 3 * blocks_per_sentence > 50000), VBS_ENOMEM, VBS_ECUDA.
+ *   *pkv is NULL on error.
+ */
 int kv_paged_init(vbs_pkv** pkv, const vbs_kv_desc* desc, int batch, int W, int blocks_per_sentence, int block,
                   int max_blocks, void* pool, vbs_stream_t stream);
 /*
@@ -283,6 +307,9 @@ int kv_paged_init(vbs_pkv** pkv, const vbs_kv_desc* desc, int batch, int W, int 
  * K/V through the table of the sentence's first row and calls
  * kv_paged_prepare(P) before the first generated position is written.
  * Synchronises the stream (the tables are built on the host, once per decode).
+ * Drops copies still pending.
+ * Errors: VBS_EINVAL (P < 0, or the prompt needs more blocks than a sentence
+ *   owns or a table row holds), VBS_ECUDA.
  */
 int kv_paged_prefill(vbs_pkv* pkv, int P);
 /*
@@ -290,6 +317,9 @@ int kv_paged_prefill(vbs_pkv* pkv, int P);
  * a row whose table ends at that block boundary gets a fresh block; of the
  * rows sharing a partly filled block the lowest keeps it and every other row
  * gets a copy of its t_write % block filled slots (copy-on-write).
+ * Errors: VBS_EINVAL (t_write < 0, or a block index beyond max_blocks),
+ *   VBS_ESTATE (copies recorded by bs_step_paged still pending), VBS_ECUDA;
+ *   an exhausted free stack is VBS_ENOMEM in kv_paged_status().
  */
 int kv_paged_prepare(vbs_pkv* pkv, int t_write);
 /*
@@ -297,8 +327,9 @@ int kv_paged_prepare(vbs_pkv* pkv, int t_write);
  * becomes row beam_idx[r]'s, counts are raised for the new references before
  * the old ones are dropped, blocks reaching zero return to their sentence's
  * stack, then kv_paged_prepare(t_valid) runs.  Two launches, no host sync.
- * Errors: VBS_EINVAL (host checks); VBS_ENOMEM / VBS_EINVAL on the device are
- * reported by kv_paged_status().
+ * Errors: VBS_EINVAL (host checks as kv_paged_prepare, NULL beam_idx),
+ * VBS_ESTATE (copies pending), VBS_ECUDA; VBS_ENOMEM / VBS_EINVAL on the device
+ * are reported by kv_paged_status().
  */
 int kv_paged_reorder(vbs_pkv* pkv, const int32_t* beam_idx, int t_valid);
 /*
@@ -322,33 +353,45 @@ int kv_paged_reorder(vbs_pkv* pkv, const int32_t* beam_idx, int t_valid);
  */
 int bs_step_paged(vbs_bs* ctx, const void* logits, int64_t ld, float* scores, int32_t* seqs, int32_t* beam_idx,
                   int32_t* tokens, int32_t* all_done, vbs_pkv* pkv, int t_valid);
-/* The copy-on-write tasks recorded by bs_step_paged (one launch; none pending: no copy). */
+/* The copy-on-write tasks recorded by bs_step_paged (one launch; none pending: no copy).
+   Errors: VBS_EINVAL (NULL), VBS_ECUDA. */
 int kv_paged_copy(vbs_pkv* pkv);
-/* The device block table [R][max_blocks] and its row stride. */
+/* The device block table [R][max_blocks] and its row stride (library-owned, valid until
+   kv_paged_destroy).  Errors: VBS_EINVAL (NULL arguments). */
 int kv_paged_table(vbs_pkv* pkv, const int32_t** table, int* max_blocks);
-/* Copy the reference counts [num_blocks] and per-row block counts [R] to device buffers (either may be NULL). */
+/* Copy the reference counts [num_blocks] and per-row block counts [R] to device buffers
+   (either may be NULL), on the stream.  Errors: VBS_EINVAL (NULL pkv), VBS_ECUDA. */
 int kv_paged_counts(vbs_pkv* pkv, int32_t* refcnt, int32_t* nblk);
-/* Copy the block table [R][max_blocks] to a device buffer (entries at or beyond a row's block count are stale). */
+/* Copy the block table [R][max_blocks] to a device buffer (entries at or beyond a row's
+   block count are stale), on the stream.  Errors: VBS_EINVAL (NULL), VBS_ECUDA. */
 int kv_paged_copy_table(vbs_pkv* pkv, int32_t* out);
 /*
  * Save / restore the allocator state (block table, block counts, reference
  * counts, free stacks) into / from the context's own copy, device to device on
  * the stream: a decode can restart from the state right after the prompt
  * without a host round trip.  Pool contents are not copied; positions the
- * restored tables do not cover are simply unused.
+ * restored tables do not cover are simply unused.  Restore drops copies still
+ * pending.  Errors: VBS_EINVAL (NULL), VBS_ECUDA.
  */
 int kv_paged_save(vbs_pkv* pkv);
 int kv_paged_restore(vbs_pkv* pkv);
 /* Synchronise the stream and return the number of filled slots copied by
    copy-on-write since init (one slot = one position of one (layer, k/v, head)
-   run: head_dim * elem_bytes bytes read and the same written). */
+   run: head_dim * elem_bytes bytes read and the same written).
+   Errors: VBS_EINVAL (NULL arguments), VBS_ECUDA. */
 int kv_paged_cow_slots(vbs_pkv* pkv, int64_t* slots);
-/* Synchronise the stream and return (then clear) the device status word. */
+/* Synchronise the stream and return (then clear) the device status word: VBS_OK or
+   the first VBS_E* a kernel recorded.  VBS_EINVAL for NULL, VBS_ECUDA when the
+   synchronisation or the read fails. */
 int kv_paged_status(vbs_pkv* pkv);
+/* Free the cache's own memory (synchronises its stream first; the pool stays the
+   caller's).  NULL is a no-op.  Returns VBS_OK. */
 int kv_paged_destroy(vbs_pkv* pkv);
 
 /* Synchronise `stream` and return (then clear) the status word of the calls
-   that have no context (kv_reorder's bounded waits). */
+   that have no context (kv_reorder's and bpd_verify's bounded waits,
+   bs_expand_static's input checks).  VBS_ECUDA when the synchronisation or the
+   read fails. */
 int vbs_stateless_status(vbs_stream_t stream);
 
 /* =============================================================================
@@ -362,7 +405,10 @@ int vbs_stateless_status(vbs_stream_t stream);
 
 /*
  * Predict: proposals[b, h] = argmax_v logits[b, h, v] for logits [B, k, V]
- * (device, dense rows); argmax ties go to the lower token id.
+ * (device, dense rows); argmax ties go to the lower token id.  proposals[B, k]
+ * int32 (device).  B = 0 launches nothing.
+ * Errors: VBS_EINVAL (B < 0, k outside 1..32, V < 1, unknown dtype, NULL
+ *   pointers with B > 0), VBS_ECUDA.
  */
 int bpd_propose(const void* logits, int B, int k, int V, int dtype, int32_t* proposals, vbs_stream_t stream);
 
@@ -379,6 +425,8 @@ int bpd_propose(const void* logits, int B, int k, int V, int dtype, int32_t* pro
  * each call's last CTA): two bpd_verify calls that overlap on the GPU
  * (different streams or host threads) race and must be serialised by the
  * caller.  A wait that gives up is reported by vbs_stateless_status().
+ * Errors: VBS_EINVAL (B < 0, k outside 1..32, V < 1, eos >= V, unknown dtype,
+ *   NULL pointers with B > 0), VBS_ECUDA.
  */
 int bpd_verify(const void* logits, const int32_t* proposals, int B, int k, int V, int dtype, int eos,
                int32_t* khat, int32_t* next, vbs_stream_t stream);
