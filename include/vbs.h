@@ -32,6 +32,9 @@
  *   - Logits are row-major with a row stride `ld` (elements) >= V; dtype is
  *     VBS_F32 or VBS_BF16.  Logits must be finite or -inf, with at least one
  *     finite value per row that is read.
+ *   - One device per process: the kernels' shared-memory attributes are set
+ *     once per process, on the device current at the first launch.  A process
+ *     that drives several GPUs runs one process per GPU (as the bench does).
  */
 #ifndef VBS_H
 #define VBS_H
