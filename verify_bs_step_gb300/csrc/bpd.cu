@@ -482,13 +482,8 @@ template <typename T, bool VECTOR, bool RANK>
 static int launch_queue(int grid, const void* logits, const int32_t* proposals, int B, int k, int V, int eos,
                         const BpdCrit& crit, int32_t* khat, int32_t* next, int* status, cudaStream_t s) {
   const int smem = VECTOR ? BPD_BUF : 0;
-  static bool attr_set = false;                  // one per kernel instantiation
-  if (VECTOR && !attr_set) {
-    if (cudaFuncSetAttribute(bpd_verify_queue_kernel<T, VECTOR, RANK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             BPD_BUF) != cudaSuccess)
-      return VBS_ECUDA;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};   // one per kernel instantiation
+  if (VECTOR && !smem_attr_once(bpd_verify_queue_kernel<T, VECTOR, RANK>, BPD_BUF, attr_done)) return VBS_ECUDA;
   bpd_verify_queue_kernel<T, VECTOR, RANK><<<grid, BPD_RT, smem, s>>>(logits, proposals, B, k, V, eos, crit, khat,
                                                                      next, status);
   return cudaGetLastError() == cudaSuccess ? VBS_OK : VBS_ECUDA;

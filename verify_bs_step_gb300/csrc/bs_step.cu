@@ -92,29 +92,37 @@ __device__ void warp_select_topk(u64* keys, int n, int K, u64* out, int lane) {
   }
 }
 
-// Number of entries of a descending list L[0..len) greater than k.
-__device__ __forceinline__ int count_gt(const u64* L, int len, u64 k) {
-  int lo = 0, hi = len;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (L[mid] > k) lo = mid + 1;
-    else hi = mid;
-  }
-  return lo;
-}
-
-// K best of nl descending lists of K keys each, by rank (binary search in the others).
+// K best of nl descending lists of K keys each (keys distinct, 0 = none), in order: K rounds
+// of a warp-wide maximum over the lists' heads; lane c walks lists c, c + 32, ...
+// (nl <= PART_KEYS / 2).
 __device__ void warp_merge_sorted(const u64* lists, int nl, int K, u64* out, int lane) {
-  if (lane < K) out[lane] = 0;
-  __syncwarp();
-  for (int f = lane; f < nl * K; f += 32) {
-    const int c = f / K, i = f - c * K;
-    const u64 k = lists[f];
-    if (k == 0) continue;
-    int rank = i;
-    for (int c2 = 0; c2 < nl && rank < K; ++c2)
-      if (c2 != c) rank += count_gt(lists + c2 * K, K, k);
-    if (rank < K) out[rank] = k;
+  constexpr int LPL = PART_KEYS / 2 / 32;
+  int pos[LPL];
+  u64 head[LPL];
+#pragma unroll
+  for (int m = 0; m < LPL; ++m) {
+    const int c = lane + 32 * m;
+    pos[m] = 0;
+    head[m] = c < nl ? lists[c * K] : 0ull;
+  }
+  for (int i = 0; i < K; ++i) {
+    u64 mine = head[0];
+#pragma unroll
+    for (int m = 1; m < LPL; ++m) mine = head[m] > mine ? head[m] : mine;
+    const u32 hi = static_cast<u32>(mine >> 32);
+    const u32 mhi = __reduce_max_sync(FULL, hi);
+    const u32 mlo = __reduce_max_sync(FULL, hi == mhi ? static_cast<u32>(mine) : 0u);
+    const u64 best = (static_cast<u64>(mhi) << 32) | mlo;
+    if (lane == 0) out[i] = best;
+    if (best != 0ull) {
+#pragma unroll
+      for (int m = 0; m < LPL; ++m) {
+        if (head[m] == best) {                 // the one list it came from moves on
+          ++pos[m];
+          head[m] = pos[m] < K ? lists[(lane + 32 * m) * K + pos[m]] : 0ull;
+        }
+      }
+    }
   }
   __syncwarp();
 }
@@ -133,6 +141,7 @@ struct BsShared {                              // the stream kernel
   u64 full[NSTAGE], empty[NSTAGE];
   u64 rbar[NSLOT];                             // the key bar of a rescan
   u32 thr[NSLOT];                              // threshold (ordered logit bits) per segment
+  u32 tmin[NSLOT];                             // first chunk: the least of the warps' ceil(K / warps)-th best
   u32 sbar[NSLOT];                             // the final bar (ordered logit bits)
   int qcnt[NSLOT];                             // entries reserved in q[slot] (> QSEG: overflow)
   int qref[NSLOT];                             // qcnt at the last threshold refresh
@@ -229,10 +238,35 @@ __device__ __forceinline__ u32 queue_bar(const BsShared& sh, int slot, int n, in
   return warp_kth_u32(lm, K, lane);
 }
 
+// Warp-wide, for lists longer than a warp's lanes make tight (K > 8): the largest x whose
+// low 32 - bits bits are zero with at least K of the first n entries' tile maxima at or
+// above it, found bit by bit from the top; with bits = 32 it is their K-th best exactly
+// (0 if fewer than K are nonzero).
+__device__ __forceinline__ u32 queue_kth(const BsShared& sh, int slot, int n, int K, int lane, int bits) {
+  constexpr int PER = QSEG / 32;
+  const volatile u64* vq = sh.q[slot];
+  u32 h[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int j = lane + 32 * i;
+    h[i] = j < n ? static_cast<u32>(vq[j] >> 32) : 0u;
+  }
+  u32 x = 0;
+  for (int b = 31; b >= 32 - bits; --b) {
+    const u32 c = x | (1u << b);
+    int cnt = 0;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) cnt += h[i] >= c ? 1 : 0;
+    if (__reduce_add_sync(FULL, static_cast<unsigned>(cnt)) >= static_cast<unsigned>(K)) x = c;
+  }
+  return x;
+}
+
 // Warp-wide: raise the segment's threshold from its queue.
+template <bool BIGK>
 __device__ __noinline__ void queue_refresh(BsShared& sh, int slot, int n, int K, int lane) {
   if (lane == 0) sh.qref[slot] = n;
-  const u32 t = queue_bar(sh, slot, n, K, lane);
+  const u32 t = BIGK ? queue_kth(sh, slot, n, K, lane, 20) : queue_bar(sh, slot, n, K, lane);
   if (lane == 0 && t) atomicMax(&sh.thr[slot], t);
 }
 
@@ -306,12 +340,12 @@ __device__ void produce(const BsArgs& a, BsShared& sh, int64_t e0, int64_t e1) {
 // maximum; the tiles reaching it are read again and every element at or above the bar
 // is collected into fin[s].  mode[s] becomes 1 when that does not fit (queue overflow,
 // more than CT_CAP tiles or FIN_CAP keys at the bar: ties, adversarial orders).
-template <typename T, int VEC>
+template <typename T, int VEC, bool BIGK>
 __device__ void resolve_tiles(const BsArgs& a, BsShared& sh, int s, int lane) {
   const int K = a.K;
   const int qn = sh.qcnt[s];
   const int n = min(qn, QSEG);
-  const u32 bar = queue_bar(sh, s, n, K, lane);
+  const u32 bar = BIGK ? queue_kth(sh, s, n, K, lane, 32) : queue_bar(sh, s, n, K, lane);
   if (lane == 0) { sh.sbar[s] = bar; sh.fcnt[s] = 0; }
   int nc = 0;
   for (int j0 = 0; j0 < n; j0 += 32) {
@@ -453,14 +487,14 @@ __device__ void finish_segment(const BsArgs& a, BsShared& sh, int s, int lane) {
   __syncwarp();
   const int n = mode == 0 ? min(sh.qcnt[s], QSEG) : QSEG;
   for (int j = lane; j < n; j += 32) sh.q[s][j] = 0ull;
-  if (lane == 0) { sh.qcnt[s] = 0; sh.qref[s] = 0; sh.thr[s] = 0u; sh.mode[s] = 0; }
+  if (lane == 0) { sh.qcnt[s] = 0; sh.qref[s] = 0; sh.thr[s] = 0u; sh.tmin[s] = 0xffffffffu; sh.mode[s] = 0; }
 }
 
 // All consumers (after a consumer barrier): publish slots [0, ns).
-template <typename T, int VEC>
+template <typename T, int VEC, bool BIGK>
 __device__ void publish_slots(const BsArgs& a, BsShared& sh, int ns) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (warp < ns && !sh.seg_skip[warp]) resolve_tiles<T, VEC>(a, sh, warp, lane);
+  if (warp < ns && !sh.seg_skip[warp]) resolve_tiles<T, VEC, BIGK>(a, sh, warp, lane);
   named_sync(BAR_CONSUMERS, BS_NC);
   for (int s = 0; s < ns; ++s)
     if (!sh.seg_skip[s] && sh.mode[s] == 1) rescan_segment<T, VEC>(a, sh, s);
@@ -470,7 +504,9 @@ __device__ void publish_slots(const BsArgs& a, BsShared& sh, int ns) {
 // The consumers: every chunk of the range, one row segment after the other.  Nothing in
 // the loop waits for another warp; segments are published after the loop (or when all
 // NSLOT slots hold one).
-template <typename T, bool TMA>
+// BIGK (the stream kernel's instance for K > 8): the threshold seed takes a second,
+// cross-warp bound and the queue's bars are computed exactly.
+template <typename T, bool TMA, bool BIGK>
 __device__ void consume(const BsArgs& a, BsShared& sh, int64_t e0, int64_t e1) {
   constexpr int VEC = TMA ? Vec16<T>::N : 1;
   constexpr int64_t SE = static_cast<int64_t>(BS_NC) * BS_U * VEC;
@@ -487,7 +523,7 @@ __device__ void consume(const BsArgs& a, BsShared& sh, int64_t e0, int64_t e1) {
       slot = seg % NSLOT;
       if (seg > 0 && slot == 0) {                   // every slot holds a segment: publish them
         named_sync(BAR_CONSUMERS, BS_NC);
-        publish_slots<T, VEC>(a, sh, NSLOT);
+        publish_slots<T, VEC, BIGK>(a, sh, NSLOT);
         named_sync(BAR_CONSUMERS, BS_NC);
       }
       if constexpr (!TMA) skip = row_skipped(a, ch.r);
@@ -548,8 +584,22 @@ __device__ void consume(const BsArgs& a, BsShared& sh, int64_t e0, int64_t e1) {
         seeded = true;
         const u32 seed = warp_kth_u32(tmo, K, lane);
         if (lane == 0 && seed > thr_o) atomicMax(&sh.thr[slot], seed);
+        if constexpr (BIGK) {
+          // a second bound: each of the BS_NCW warps has j = ceil(K / BS_NCW) lane maxima
+          // at or above its own j-th best, so at least K tiles reach the least of those
+          // (with K > 8 the warps' K-th bests alone let most of the chunk's tiles in)
+          const u32 seed_j = warp_kth_u32(tmo, (K + BS_NCW - 1) / BS_NCW, lane);
+          if (lane == 0) atomicMin(&sh.tmin[slot], seed_j);
+        }
         named_sync(BAR_CONSUMERS, BS_NC);
         thr_o = *reinterpret_cast<volatile u32*>(&sh.thr[slot]);
+        if constexpr (BIGK) {
+          const u32 mn = *reinterpret_cast<volatile u32*>(&sh.tmin[slot]);
+          if (mn > thr_o) {
+            thr_o = mn;
+            if (lane == 0) atomicMax(&sh.thr[slot], mn);
+          }
+        }
       }
       if (tmo != 0u && tmo >= thr_o) {
         // also record where the maximum sits (vector um, element em) and a bound on the
@@ -622,7 +672,7 @@ __device__ void consume(const BsArgs& a, BsShared& sh, int64_t e0, int64_t e1) {
       if (warp == (c & (BS_NCW - 1))) {
         const int nq = __shfl_sync(FULL, *reinterpret_cast<volatile int*>(&sh.qcnt[slot]), 0);
         const int nr = __shfl_sync(FULL, *reinterpret_cast<volatile int*>(&sh.qref[slot]), 0);
-        if (nq >= nr + QSTEP) queue_refresh(sh, slot, nq < QSEG ? nq : QSEG, K, lane);
+        if (nq >= nr + QSTEP) queue_refresh<BIGK>(sh, slot, nq < QSEG ? nq : QSEG, K, lane);
       }
     }
     if (ch.last) {
@@ -637,14 +687,14 @@ __device__ void consume(const BsArgs& a, BsShared& sh, int64_t e0, int64_t e1) {
     }
   }
   named_sync(BAR_CONSUMERS, BS_NC);
-  if (seg >= 0) publish_slots<T, VEC>(a, sh, slot + 1);
+  if (seg >= 0) publish_slots<T, VEC, BIGK>(a, sh, slot + 1);
 }
 
 // ---------------------------------------------------------------------------------------
 // the stream kernel
 // ---------------------------------------------------------------------------------------
 
-template <typename T, bool TMA>
+template <typename T, bool TMA, bool BIGK>
 __global__ void __launch_bounds__(BS_NT, 1) bs_stream_kernel(const BsArgs a) {
   extern __shared__ __align__(128) unsigned char bs_smem[];
   BsShared& sh = *reinterpret_cast<BsShared*>(bs_smem);
@@ -661,6 +711,7 @@ __global__ void __launch_bounds__(BS_NT, 1) bs_stream_kernel(const BsArgs a) {
     }
     if (threadIdx.x < NSLOT) {
       sh.thr[threadIdx.x] = 0u;
+      sh.tmin[threadIdx.x] = 0xffffffffu;
       sh.qcnt[threadIdx.x] = 0;
       sh.qref[threadIdx.x] = 0;
       sh.mode[threadIdx.x] = 0;
@@ -672,7 +723,7 @@ __global__ void __launch_bounds__(BS_NT, 1) bs_stream_kernel(const BsArgs a) {
         if ((threadIdx.x & 31) == 0) produce<T>(a, sh, e0, e1);
       }
     } else {
-      consume<T, TMA>(a, sh, e0, e1);
+      consume<T, TMA, BIGK>(a, sh, e0, e1);
     }
   }
   // the merge grid may start filling the SMs this CTA leaves
@@ -948,6 +999,7 @@ __global__ void __launch_bounds__(BS_NT, 1) bs_cluster_kernel(const BsArgs a) {
   }
   if (threadIdx.x < NSLOT) {
     sh.thr[threadIdx.x] = 0u;
+    sh.tmin[threadIdx.x] = 0xffffffffu;
     sh.qcnt[threadIdx.x] = 0;
     sh.qref[threadIdx.x] = 0;
     sh.mode[threadIdx.x] = 0;
@@ -975,7 +1027,7 @@ __global__ void __launch_bounds__(BS_NT, 1) bs_cluster_kernel(const BsArgs a) {
     }
   } else {
     if (c == 0 && threadIdx.x < 32) cluster_prefetch(a, sh, b, threadIdx.x);
-    consume<T, TMA>(a, sh, e0, e1);
+    consume<T, TMA, false>(a, sh, e0, e1);
   }
   __syncwarp();
   cooperative_groups::this_cluster().sync();       // every CTA's row results are in its shared memory
@@ -1390,30 +1442,28 @@ __global__ void bs_finalize_kernel(const BsArgs a, const float* scores, const in
 // host launchers
 // ---------------------------------------------------------------------------------------
 
+template <typename T, bool TMA, bool BIGK>
+static int launch_stream_k(const BsArgs& a, int grid, cudaStream_t s) {
+  static std::atomic<unsigned long long> attr_done{0};
+  const int smem = static_cast<int>(sizeof(BsShared));
+  if (!smem_attr_once(bs_stream_kernel<T, TMA, BIGK>, smem, attr_done)) return VBS_ECUDA;
+  bs_stream_kernel<T, TMA, BIGK><<<grid, BS_NT, smem, s>>>(a);
+  return cudaGetLastError() == cudaSuccess ? VBS_OK : VBS_ECUDA;
+}
+
+// K > 8 (W > 4) takes the instance with the cross-warp seed and exact queue bars; the
+// smaller lists keep the lighter loop.
 template <typename T, bool TMA>
 static int launch_stream(const BsArgs& a, int grid, cudaStream_t s) {
-  static bool attr_set = false;
-  const int smem = static_cast<int>(sizeof(BsShared));
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(bs_stream_kernel<T, TMA>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-        cudaSuccess)
-      return VBS_ECUDA;
-    attr_set = true;
-  }
-  bs_stream_kernel<T, TMA><<<grid, BS_NT, smem, s>>>(a);
-  return cudaGetLastError() == cudaSuccess ? VBS_OK : VBS_ECUDA;
+  return a.K > 8 ? launch_stream_k<T, TMA, true>(a, grid, s) : launch_stream_k<T, TMA, false>(a, grid, s);
 }
 
 // The merge grid is a programmatic dependent of the stream grid: it may launch
 // while the stream CTAs retire and waits for their writes in griddepcontrol.wait.
 static int launch_merge(const BsArgs& a, cudaStream_t s) {
-  static bool attr_set = false;
+  static std::atomic<unsigned long long> attr_done{0};
   const int smem = static_cast<int>(sizeof(MergeShared));
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(bs_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-      return VBS_ECUDA;
-    attr_set = true;
-  }
+  if (!smem_attr_once(bs_merge_kernel, smem, attr_done)) return VBS_ECUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.B);
   cfg.blockDim = dim3(MG_NT);
@@ -1429,14 +1479,9 @@ static int launch_merge(const BsArgs& a, cudaStream_t s) {
 
 template <typename T, bool TMA, bool FUSE>
 static int launch_cluster(const BsArgs& a, cudaStream_t s) {
-  static bool attr_set = false;
+  static std::atomic<unsigned long long> attr_done{0};
   const int smem = static_cast<int>(sizeof(BsShared));
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(bs_cluster_kernel<T, TMA, FUSE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-        cudaSuccess)
-      return VBS_ECUDA;
-    attr_set = true;
-  }
+  if (!smem_attr_once(bs_cluster_kernel<T, TMA, FUSE>, smem, attr_done)) return VBS_ECUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.B * a.cluster);
   cfg.blockDim = dim3(BS_NT);
@@ -1846,14 +1891,9 @@ int launch_bs_expand_static(BsArgs a, int grid, bool vector_ok, float* scores_ou
     st = vector_ok ? launch_stream<float, true>(a, grid, s) : launch_stream<float, false>(a, grid, s);
   if (st != VBS_OK) return st;
 
-  static bool attr_set = false;
+  static std::atomic<unsigned long long> attr_done{0};
   const int smem = static_cast<int>(sizeof(MergeShared));
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(bs_expand_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-        cudaSuccess)
-      return VBS_ECUDA;
-    attr_set = true;
-  }
+  if (!smem_attr_once(bs_expand_merge_kernel, smem, attr_done)) return VBS_ECUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.B);
   cfg.blockDim = dim3(MG_NT);

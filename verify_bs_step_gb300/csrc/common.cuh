@@ -2,6 +2,7 @@
 #pragma once
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -265,6 +266,19 @@ template <int N> __device__ __forceinline__ void bulk_wait() {
 
 __device__ __forceinline__ void set_status(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
+}
+
+// Raise a kernel's dynamic shared-memory limit once per device (the attribute is per
+// device and function); `done` holds one bit per device already set.
+template <typename F>
+inline bool smem_attr_once(F* fn, int bytes, std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  const unsigned long long bit = 1ull << dev;
+  if (done.load(std::memory_order_acquire) & bit) return true;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
+  done.fetch_or(bit, std::memory_order_acq_rel);
+  return true;
 }
 
 }  // namespace vbs

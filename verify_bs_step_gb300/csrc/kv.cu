@@ -138,12 +138,8 @@ int launch_kv_naive(const KvGeom& g, const void* src, void* dst, const int32_t* 
                g.seg_stride, g.copy_bytes, (g.copy_bytes + KV_CHUNK - 1) / KV_CHUNK};
     const int64_t n_items = n_segs * m.nch;
     const size_t smem = static_cast<size_t>(KV_STAGES) * KV_CHUNK;
-    static bool attr_set = false;
-    if (!attr_set) {
-      cudaFuncSetAttribute(kv_naive_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem));
-      attr_set = true;
-    }
+    static std::atomic<unsigned long long> attr_done{0};
+    if (!smem_attr_once(kv_naive_bulk_kernel, static_cast<int>(smem), attr_done)) return VBS_ECUDA;
     const int grid = static_cast<int>(std::min<int64_t>(n_items, static_cast<int64_t>(num_sms) * KV_CTAS_PER_SM));
     kv_naive_bulk_kernel<<<grid, 32, smem, s>>>(m, n_items, status);
   } else {
