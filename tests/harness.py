@@ -7,20 +7,17 @@ decision the oracle takes has a scaled gap >= MIN_GAP (see oracle.beam._gap:
 Sentences the oracle does not check keep salt 0 and are generated on the
 device.  No value computed by the CUDA path ever feeds the oracle.
 
-Score tolerance, derived from the arithmetic: the kernel forms each candidate
-in fp32 as s + ((x - hi) - lo), from the fp32 cumulative score s, the exact
-logit x and the row LSE carried as an fp32 pair hi + lo; the LSE's fp32
-partial sums carry a relative error of about 1e-6 (about 1e-6 absolute at
-|LSE| ~ 10), the subtraction x - hi rounds by at most half an ulp of ~30
-(1e-6), and the new score rounds by half an ulp (6e-8 |s|).  Over t steps the
-score therefore drifts by at most sum_i (6e-8 |s_i| + 2e-6) <= 3e-8 t |s_t| +
-2e-6 t.  The test allows  |gpu - ref| <= 1e-5 |ref| + 4e-6 t  (the relative
-part holds the drift for t <= 300, the absolute part covers the per-step error
-with a factor 2).
+Score tolerance: every finite score (cumulative scores, normalised scores of
+finished hypotheses and of the final choice) must satisfy
+|gpu - ref| <= 1e-5 |ref|, the relative bound stated for this path; a score
+whose reference is 0 or infinite must be equal.  Each comparison records its
+relative error in ``REL_ERR`` (worst value per test), which the test session
+prints at its end, so the margin left under the bound is visible.
 """
 
 from __future__ import annotations
 
+import dataclasses
 import math
 from dataclasses import dataclass, field
 
@@ -32,11 +29,32 @@ from oracle import beam as ob
 
 MIN_GAP = 1e-3
 REL_TOL = 1e-5
-ABS_TOL_PER_STEP = 4e-6
+
+# worst relative score error seen per test: {test id: (error, where)}; the session prints it
+REL_ERR: dict = {}
+CURRENT_TEST = ["(outside a test)"]
 
 
-def score_tol(ref, t):
-    return REL_TOL * np.abs(ref) + ABS_TOL_PER_STEP * t
+def score_tol(ref, t=None):
+    """The allowed |gpu - ref| for finite references (t is unused: the bound is purely relative)."""
+    return REL_TOL * np.abs(ref)
+
+
+def check_scores(got, ref, what: str):
+    """Assert the relative bound on every finite score, equality on the rest; record the worst error."""
+    got = np.asarray(got, dtype=np.float64).reshape(-1)
+    ref = np.asarray(ref, dtype=np.float64).reshape(-1)
+    exact = ~np.isfinite(ref) | (ref == 0)
+    assert (got[exact] == ref[exact]).all(), f"{what}: non-finite or zero scores differ: {got[exact]} vs {ref[exact]}"
+    fin = ~exact
+    if not fin.any():
+        return
+    rel = np.abs(got[fin] - ref[fin]) / np.abs(ref[fin])
+    worst = float(rel.max())
+    key = CURRENT_TEST[0]
+    if worst > REL_ERR.get(key, (-1.0, ""))[0]:
+        REL_ERR[key] = (worst, what)
+    assert worst <= REL_TOL, f"{what}: relative score error {worst:.3g} > {REL_TOL:g} (ref {ref[fin]}, got {got[fin]})"
 
 
 @dataclass
@@ -83,7 +101,8 @@ def _rows(case: BeamCase, b: int, step: int, salt: int, bias, device="cpu"):
                              dtype=case.dtype, eos=case.eos, bias=bias, device=device)
 
 
-def run_oracle(case: BeamCase, min_gap: float = MIN_GAP, max_salts: int = 200) -> OracleTrace:
+def run_oracle(case: BeamCase, min_gap: float = MIN_GAP, max_salts: int = 200,
+               stop_when_done: bool = True) -> OracleTrace:
     checked = list(range(case.B)) if case.checked is None else list(case.checked)
     bias = synth.zipf_bias(case.V, case.seed) if case.kind == "llama" else None
     bs = ob.BeamSearch(len(checked), case.W, case.V, eos=case.eos, alpha=case.alpha,
@@ -112,8 +131,86 @@ def run_oracle(case: BeamCase, min_gap: float = MIN_GAP, max_salts: int = 200) -
         tr.seqs.append([list(s) for s in bs.seqs])
         tr.hyps.append([h.copy() for h in bs.hyps])
         tr.done.append(bs.done.copy())
-        if res.all_done:
+        if res.all_done and stop_when_done:
             break
+    return tr
+
+
+_POOL: list = []
+
+
+def _pool_init():
+    torch.set_num_threads(1)
+
+
+def _oracle_pool():
+    """One pool of spawned worker processes (one per host core) for the whole session: spawned,
+    not forked, because the test process holds a CUDA context; the workers use the CPU only."""
+    import atexit
+    import multiprocessing as mp
+    import os
+
+    if not _POOL:
+        size = max(1, os.cpu_count() or 1)
+        pool = mp.get_context("spawn").Pool(size, initializer=_pool_init)
+        atexit.register(pool.terminate)
+        _POOL.append((pool, size))
+    return _POOL[0]
+
+
+def _oracle_chunk(job):
+    case, chunk, min_gap, max_salts = job
+    return run_oracle(dataclasses.replace(case, checked=list(chunk)), min_gap, max_salts, stop_when_done=False)
+
+
+def run_oracle_parallel(case: BeamCase, workers: int | None = None, min_gap: float = MIN_GAP,
+                        max_salts: int = 200) -> OracleTrace:
+    """run_oracle over the checked sentences split across spawned worker processes.
+
+    Sentences are independent, so each worker runs the oracle on a contiguous chunk for
+    every step; the chunks' traces are joined sentence-wise and cut at the first step
+    where every sentence is done, which is the trace run_oracle gives for the whole set.
+    """
+    checked = list(range(case.B)) if case.checked is None else list(case.checked)
+    pool, size = _oracle_pool()
+    n = max(1, min(workers or size, len(checked)))
+    bounds = [round(i * len(checked) / n) for i in range(n + 1)]
+    chunks = [checked[bounds[i]:bounds[i + 1]] for i in range(n) if bounds[i + 1] > bounds[i]]
+    parts = pool.map(_oracle_chunk, [(case, c, min_gap, max_salts) for c in chunks], chunksize=1)
+    T = len(parts[0].steps)
+    L = next((t + 1 for t in range(T) if all(p.steps[t].all_done for p in parts)), T)
+    W = case.W
+    bs = ob.BeamSearch(len(checked), W, case.V, eos=case.eos, alpha=case.alpha,
+                       early_stopping=case.early_stopping, lp_kind=case.lp_kind, max_len=case.ML,
+                       bos=case.bos, pad=case.pad)
+    tr = OracleTrace(bs, checked)
+    for t in range(L):
+        off, bi, tok, sc, dn, sents, salts = 0, [], [], [], [], {}, {}
+        seqs, hyps = [], []
+        for p in parts:
+            r = p.steps[t]
+            bi.append(np.where(r.beam_idx >= 0, r.beam_idx + off * W, -1))
+            tok.append(r.tokens)
+            sc.append(r.scores)
+            dn.append(r.done)
+            sents.update({off + b: ss for b, ss in r.sentences.items()})
+            salts.update(p.salts[t])
+            seqs.extend(p.seqs[t])
+            hyps.extend(p.hyps[t])
+            off += len(p.checked)
+        done = np.concatenate(dn)
+        tr.steps.append(ob.StepResult(np.concatenate(bi), np.concatenate(tok), np.concatenate(sc), done,
+                                      bool(done.all()), sents))
+        tr.salts.append(salts)
+        tr.seqs.append(seqs)
+        tr.hyps.append(hyps)
+        tr.done.append(done.copy())
+    last = tr.steps[L - 1]
+    bs.scores = last.scores.reshape(len(checked), W).copy()
+    bs.seqs = [list(s) for s in tr.seqs[L - 1]]
+    bs.done = tr.done[L - 1].copy()
+    bs.hyps = [h.copy() for h in tr.hyps[L - 1]]
+    bs.t = L
     return tr
 
 
@@ -143,12 +240,7 @@ def compare_step(case, tr: OracleTrace, t: int, gpu_bi, gpu_tok, gpu_sc, gpu_seq
         exp_bi = np.where(ref_bi >= 0, ref_bi - i * W + b * W, -1)    # local -> global rows
         np.testing.assert_array_equal(gpu_bi[g], exp_bi, err_msg=f"beam_idx step {t} sentence {b}")
         np.testing.assert_array_equal(gpu_tok[g], res.tokens[o], err_msg=f"tokens step {t} sentence {b}")
-        ref = res.scores[o]
-        err = np.abs(gpu_sc[g].astype(np.float64) - ref)
-        fin = np.isfinite(ref)
-        assert (gpu_sc[g][~fin] == ref[~fin]).all(), f"non-finite scores step {t} sentence {b}"
-        assert (err[fin] <= score_tol(ref[fin], t)).all(), \
-            f"scores step {t} sentence {b}: max err {err[fin].max()} ref {ref}"
+        check_scores(gpu_sc[g], res.scores[o], f"scores step {t} sentence {b}")
         if gpu_seqs is not None:
             for w in range(W):
                 exp = tr.seqs[t - 1][i * W + w]
@@ -174,10 +266,7 @@ def compare_finished(case, tr: OracleTrace, fin: dict, t: int):
             assert ser[r] == hy.serial, f"serial sentence {b}"
             assert ln[r] == hy.length, f"|y| sentence {b}"
             np.testing.assert_array_equal(tok[r, :len(hy.tokens)], hy.tokens, err_msg=f"hyp tokens sentence {b}")
-            if math.isfinite(hy.ns):
-                assert abs(ns[r] - hy.ns) <= score_tol(hy.ns, t), f"ns sentence {b}: {ns[r]} vs {hy.ns}"
-            else:
-                assert ns[r] == hy.ns
+            check_scores([ns[r]], [hy.ns], f"finished ns sentence {b} step {t}")
 
 
 def run_gpu_case(case: BeamCase, tr: OracleTrace, device="cuda", check_every_step=True, two_pass=False,
@@ -223,7 +312,4 @@ def compare_finalize(case, tr: OracleTrace, bs, n_return: int = 1):
             g, o = b * n + j, i * n + j
             np.testing.assert_array_equal(out[g], ref_out[o], err_msg=f"final row sentence {b} rank {j}")
             assert out_len[g] == ref_len[o]
-            if math.isfinite(ref_score[o]):
-                assert abs(out_score[g] - ref_score[o]) <= score_tol(ref_score[o], T) + 1e-7 * abs(ref_score[o])
-            else:
-                assert out_score[g] == ref_score[o]
+            check_scores([out_score[g]], [ref_score[o]], f"final score sentence {b} rank {j}")

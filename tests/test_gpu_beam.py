@@ -26,8 +26,8 @@ def lib():
     return vbs.lib()
 
 
-def _run(case, finalize=True, every=True):
-    tr = hz.run_oracle(case)
+def _run(case, finalize=True, every=True, parallel=False):
+    tr = hz.run_oracle_parallel(case) if parallel else hz.run_oracle(case)
     bs = hz.run_gpu_case(case, tr, check_every_step=every)
     if finalize:
         hz.compare_finalize(case, tr, bs)
@@ -233,10 +233,24 @@ def test_sweep_alpha_early_stopping(es, alpha):
 # ------------------------------------------------------------------------------------
 
 def test_tbase_full_size():
-    """batch 128, W 4, V 32000 bf16 N(0,3) + one +8 spike per row, EOS 2, 64 steps (a sample checked)."""
-    case = hz.BeamCase("tbase", 128, 4, 32000, 64, torch.bfloat16, eos=2, alpha=0.6, seed=1235,
-                       checked=[0, 1, 37, 64, 127])
-    _run(case, every=False)
+    """batch 128, W 4, V 32000 bf16 N(0,3) + one +8 spike per row, EOS 2, 64 steps; every
+    sentence checked at every step (the oracle runs in a process pool)."""
+    case = hz.BeamCase("tbase", 128, 4, 32000, 64, torch.bfloat16, eos=2, alpha=0.6, seed=1235)
+    tr = hz.run_oracle_parallel(case)
+    bs = hz.run_gpu_case(case, tr, check_every_step=True)
+    hz.compare_finalize(case, tr, bs)
+    hz.compare_finalize(case, tr, bs, n_return=case.W)
+    bs.close()
+
+
+def test_llama_full_size_every_sentence():
+    """batch 64, W 4, V 128256 bf16 N(0,2.5) + Zipf bias: all 64 sentences checked at every one
+    of the first 24 steps (the oracle runs in a process pool)."""
+    case = hz.BeamCase("llama", 64, 4, 128256, 24, torch.bfloat16, eos=2, alpha=0.6, seed=1236, max_len=200)
+    tr = hz.run_oracle_parallel(case)
+    bs = hz.run_gpu_case(case, tr, check_every_step=True)
+    hz.compare_finalize(case, tr, bs)
+    bs.close()
 
 
 def test_llama_full_size():
@@ -253,10 +267,23 @@ def test_sweep_grid(B, W, V, dtype):
     """The large-vocabulary wide-beam grid, ~2% planted EOS hits per row and step."""
     big = B * W * V > 50_000_000
     steps = 4 if big else 12
-    checked = [0] if B == 1 else [0, B - 1]
+    checked = [0] if B == 1 else [0, B // 3, 2 * B // 3, B - 1]
     case = hz.BeamCase("sweep", B, W, V, steps, dtype, eos=11, alpha=0.6, seed=B + W + V,
                        checked=checked)
     _run(case, every=not big)
+
+
+@pytest.mark.parametrize("alpha,es", [(0.0, ob.ES_TRUE), (0.0, ob.ES_NEVER), (1.0, ob.ES_TRUE), (1.0, ob.ES_NEVER)])
+@pytest.mark.parametrize("W,V,dtype", [
+    (W, V, dt) for W in (1, 4, 16) for V in (32000, 128256, 256000) for dt in (torch.float32, torch.bfloat16)])
+def test_sweep_corner_alpha_early_stopping(W, V, dtype, alpha, es):
+    """Every (W, V, dtype) corner of the sweep under alpha in {0, 1} x early_stopping in
+    {True, never}, 32 sentences with 4 checked at every step; the recipe's 50 steps where the
+    oracle is quick (so that finished sets fill and the stopping rules decide), fewer above."""
+    steps = 50 if W * V <= 600_000 else (12 if W * V <= 2_100_000 else 6)
+    case = hz.BeamCase("sweep", 32, W, V, steps, dtype, eos=11, alpha=alpha, early_stopping=es,
+                       seed=9000 + W * 7 + V % 997 + int(alpha * 3) + es * 11, checked=[0, 11, 22, 31])
+    _run(case, every=True, parallel=True)
 
 
 # ------------------------------------------------------------------------------------
