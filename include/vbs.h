@@ -235,11 +235,12 @@ int bs_destroy(vbs_bs* ctx);
  *   scores_in  [batch*W] device fp32 cumulative scores; a row at -inf is not read
  *   scores_out [batch*W] device fp32 new scores (may equal scores_in)
  *   beam_idx   [batch*W] device int32 global parent row; tokens [batch*W] int32
- * Scratch: a static device array of 4 MiB (the partial sums, partial top-K
+ * Scratch: a static device array of 4.5 MiB (the partial sums, partial top-K
  * lists and row maps), which every process that loads the library holds on
- * each device it uses until it exits.  Limit: batch*W <= 8192 rows (then the
- * scratch always fits), 1 <= W <= 16, V >= 2, batch*W*V < 2^31; larger
- * problems return VBS_ESCRATCH before anything is launched.
+ * each device it uses until it exits.  Limit: batch*W <= 8192 rows, for any
+ * 1 <= W <= 16 (the largest problem, 8192 rows at W = 16, needs 4,392,960
+ * bytes of it), V >= 2, batch*W*V < 2^31; more rows return VBS_ESCRATCH
+ * before anything is launched.
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
  * capture.  The call allocates nothing and frees nothing.  Every call shares
@@ -450,6 +451,32 @@ int bpd_verify(const void* logits, const int32_t* proposals, int B, int k, int V
  */
 int bpd_verify_approx(const void* logits, const int32_t* proposals, int B, int k, int V, int dtype, int eos,
                       int criterion, int param, int min_accept, int32_t* khat, int32_t* next, vbs_stream_t stream);
+
+/* =============================================================================
+ * In-run memory peaks.  The pages have no counterpart: these measure, on the
+ * running GPU, the bandwidth a roofline of the calls above is read against.
+ * ============================================================================= */
+
+/*
+ * Copy `bytes` from src to dst (device, non-overlapping) with 16-byte vector
+ * loads and stores, `grid` CTAs each taking one contiguous, equal share.  The
+ * bandwidth is 2 * bytes / time (read + write).
+ * Errors: VBS_EINVAL (NULL, bytes <= 0, grid outside 1..65535), VBS_EALIGN
+ *   (a pointer not 16-byte aligned, bytes not a multiple of 16), VBS_ECUDA.
+ */
+int vbs_peak_copy(const void* src, void* dst, int64_t bytes, int grid, vbs_stream_t stream);
+/*
+ * Read `bytes` from src (device) and fold a maximum over them, `grid` CTAs each
+ * taking one contiguous, equal share: mode 0 with 16-byte vector loads, mode 1
+ * through a ring of bulk copies into shared memory (one producer lane, 16
+ * consumer warps; the beam step's streaming pattern without its arithmetic).
+ * sink[grid] (device uint32) receives one word per CTA, so no load is dead
+ * code; its value carries no meaning.  A bounded wait that gives up is reported
+ * by vbs_stateless_status().
+ * Errors: VBS_EINVAL (NULL, bytes <= 0, grid outside 1..65535, unknown mode),
+ *   VBS_EALIGN (src not 16-byte aligned, bytes not a multiple of 16), VBS_ECUDA.
+ */
+int vbs_peak_read(const void* src, int64_t bytes, int grid, int mode, uint32_t* sink, vbs_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -68,6 +68,8 @@ SIGNATURES = {
     "bpd_verify": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _vp]),
     "bpd_verify_approx": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp,
                                    _vp]),
+    "vbs_peak_copy": (_c_int, [_vp, _vp, _c_i64, _c_int, _vp]),
+    "vbs_peak_read": (_c_int, [_vp, _c_i64, _c_int, _c_int, _vp, _vp]),
 }
 
 _LIB = None
@@ -284,6 +286,11 @@ def bs_expand_static(logits: torch.Tensor, scores_in: torch.Tensor, W: int, scor
         beam_idx = torch.empty(R, dtype=torch.int32, device=dev)
     if tokens is None:
         tokens = torch.empty(R, dtype=torch.int32, device=dev)
+    # the kernels read and write R contiguous entries of each on the logits' device
+    for name, t in (("scores_in", scores_in), ("scores_out", scores_out), ("beam_idx", beam_idx),
+                    ("tokens", tokens)):
+        if t.numel() != R or not t.is_contiguous() or t.device != dev:
+            raise ValueError(f"{name} must be a contiguous tensor of {R} entries on {dev}")
     _check(lib().bs_expand_static(_dev_ptr(logits, "logits"), logits.stride(0), R // W, W, V,
                                   _dtype_code(logits.dtype), _dev_ptr(scores_in, "scores_in", torch.float32),
                                   _dev_ptr(scores_out, "scores_out", torch.float32),
@@ -291,6 +298,23 @@ def bs_expand_static(logits: torch.Tensor, scores_in: torch.Tensor, W: int, scor
                                   _dev_ptr(tokens, "tokens", torch.int32), _stream(dev)),
            "bs_expand_static")
     return beam_idx, tokens, scores_out
+
+
+def peak_copy(src: torch.Tensor, dst: torch.Tensor, grid: int):
+    """Copy src's bytes into dst with the library's vector-copy kernel (`grid` CTAs)."""
+    if not (src.is_contiguous() and dst.is_contiguous()) or src.nbytes != dst.nbytes:
+        raise ValueError("src and dst must be contiguous and of equal size")
+    _check(lib().vbs_peak_copy(_dev_ptr(src, "src"), _dev_ptr(dst, "dst"), src.nbytes, grid, _stream(src.device)),
+           "vbs_peak_copy")
+
+
+def peak_read(src: torch.Tensor, grid: int, mode: int, sink: torch.Tensor):
+    """Read src's bytes with the library's read-only streaming kernel (mode 0: vector loads,
+    mode 1: bulk-copy ring); sink is an int32 tensor of at least `grid` entries."""
+    if not src.is_contiguous() or sink.numel() < grid or sink.dtype != torch.int32:
+        raise ValueError("src must be contiguous; sink int32 with >= grid entries")
+    _check(lib().vbs_peak_read(_dev_ptr(src, "src"), src.nbytes, grid, mode, _dev_ptr(sink, "sink"),
+                               _stream(src.device)), "vbs_peak_read")
 
 
 class _KvDesc(ctypes.Structure):

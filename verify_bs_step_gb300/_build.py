@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build", "vbs")
 LIB = os.path.join(HERE, "libvbs.so")
 
-SOURCES = ["api.cu", "bs_step.cu", "kv.cu", "bpd.cu"]
+SOURCES = ["api.cu", "bs_step.cu", "kv.cu", "bpd.cu", "peak.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr",
          "-Xcompiler", "-fPIC,-fvisibility=hidden", "-I", INCLUDE, "-I", CSRC]

@@ -167,6 +167,8 @@ VBS_EXPORT int bs_init(vbs_bs** out, int batch, int W, int V, int eos, double al
     a.row_one = cv.take<int>(R);
     a.row_p0 = cv.take<int>(R);
     a.row_np = cv.take<int>(R);
+    a.sent_np = cv.take<int>(batch);
+    a.sent_ticket = cv.take<int>(batch);
     a.done_count = cv.take<int>(1);
     a.all_done_dev = cv.take<int32_t>(1);
     a.status = cv.take<int>(1);
@@ -192,14 +194,27 @@ VBS_EXPORT int bs_init(vbs_bs** out, int batch, int W, int V, int eos, double al
     }
   }
   // which CTAs hold each row: row r spans elements [r V, (r + 1) V) of the flat split
-  std::vector<int> p0(R), np(R);
+  std::vector<int> p0(R), np(R), snp(batch, 0);
   for (int64_t r = 0; r < R; ++r) {
     p0[r] = static_cast<int>((r * V) / per);
     np[r] = static_cast<int>(((r + 1) * V - 1) / per - (r * V) / per + 1);
+    snp[r / W] += np[r];
   }
+  // the flat kernel: each CTA merges the sentences it completes, at most as many as its
+  // range touches
+  int64_t most = 0;
+  for (int64_t g = 0; g < G; ++g) {
+    const int64_t e0 = g * per, e1 = std::min(e0 + per, total);
+    most = std::max(most, ((e1 - 1) / V) / W - (e0 / V) / W + 1);
+  }
+  const bool flat_fits = most <= vbs::bs_flat_pend_cap();
+  a.flat = 0;                        // measured slower than the cluster and two-kernel paths so far
+  (void)flat_fits;
   bool ok = cudaMemsetAsync(c->dev_block, 0, cv.off, c->stream) == cudaSuccess;
   ok = ok && cudaMemcpyAsync(a.row_p0, p0.data(), R * sizeof(int), cudaMemcpyHostToDevice, c->stream) == cudaSuccess;
   ok = ok && cudaMemcpyAsync(a.row_np, np.data(), R * sizeof(int), cudaMemcpyHostToDevice, c->stream) == cudaSuccess;
+  ok = ok && cudaMemcpyAsync(a.sent_np, snp.data(), batch * sizeof(int), cudaMemcpyHostToDevice, c->stream) ==
+             cudaSuccess;
   const std::vector<int> ones(R, 1);
   ok = ok && cudaMemcpyAsync(a.row_one, ones.data(), R * sizeof(int), cudaMemcpyHostToDevice, c->stream) == cudaSuccess;
   ok = ok && cudaStreamSynchronize(c->stream) == cudaSuccess;
@@ -722,4 +737,22 @@ VBS_EXPORT int bpd_verify_approx(const void* logits, const int32_t* proposals, i
 VBS_EXPORT int bpd_verify(const void* logits, const int32_t* proposals, int B, int k, int V, int dtype, int eos,
                           int32_t* khat, int32_t* next, vbs_stream_t stream) {
   return bpd_verify_approx(logits, proposals, B, k, V, dtype, eos, VBS_BPD_EXACT, 0, 1, khat, next, stream);
+}
+
+// =====================================================================================
+// in-run memory peaks
+// =====================================================================================
+
+VBS_EXPORT int vbs_peak_copy(const void* src, void* dst, int64_t bytes, int grid, vbs_stream_t stream) {
+  if (!src || !dst || bytes <= 0 || grid < 1 || grid > 65535) return VBS_EINVAL;
+  if (!aligned16(src) || !aligned16(dst) || bytes % 16 != 0) return VBS_EALIGN;
+  return vbs::launch_peak_copy(src, dst, bytes, grid, reinterpret_cast<cudaStream_t>(stream));
+}
+
+VBS_EXPORT int vbs_peak_read(const void* src, int64_t bytes, int grid, int mode, uint32_t* sink, vbs_stream_t stream) {
+  if (!src || !sink || bytes <= 0 || grid < 1 || grid > 65535 || (mode != 0 && mode != 1)) return VBS_EINVAL;
+  if (!aligned16(src) || bytes % 16 != 0) return VBS_EALIGN;
+  int* status = nullptr;
+  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_stateless_status) != cudaSuccess) return VBS_ECUDA;
+  return vbs::launch_peak_read(src, bytes, grid, mode, sink, status, reinterpret_cast<cudaStream_t>(stream));
 }

@@ -65,6 +65,9 @@ struct BsArgs {
   int* row_np;                    // [R] the number of CTAs (partials) holding row r
   int* done_count;                // sentences finished (step-local counter)
   int cluster;                    // 0: flat split + merge kernel; C: a cluster of C CTAs per sentence
+  int flat;                       // 1: bs_step runs the flat kernel (merges by per-sentence tickets)
+  int* sent_np;                   // [B] row segments of sentence b in the flat split (tickets per step)
+  int* sent_ticket;               // [B] segments published this step (reset by the merging CTA)
   int* done;
   // finished sets
   double* fin_ns;
@@ -94,10 +97,13 @@ int launch_bs_finalize(const BsArgs& a, const float* scores, const int32_t* seqs
                        int32_t* out_len, float* out_score, cudaStream_t s);
 constexpr int BS_NSLOT = 4;       // row segments one stream CTA holds (cluster mode: W / C <= this)
 int bs_threads_per_cta();
+int bs_flat_pend_cap();           // sentences one flat-kernel CTA can merge
 int bs_ctas_per_sm();
 
-// bs_expand_static: scratch in a static device array of this size; rows at most
-constexpr size_t STATIC_SCRATCH_BYTES = size_t{4} << 20;
+// bs_expand_static: scratch in a static device array of this size; rows at most.  With
+// R >= the CTA count every row has P = 2 partial slots, so the carve is at most
+// R * (2 * (8 + 8 K) + 8) + 4 B bytes plus alignment: 4,392,960 at R = 8192, W = 16 (K = 32).
+constexpr size_t STATIC_SCRATCH_BYTES = size_t{9} << 19;   // 4.5 MiB
 constexpr int STATIC_MAX_ROWS = 8192;
 int launch_bs_expand_static(BsArgs a, int grid, bool vector_ok, float* scores_out, cudaStream_t s);
 
@@ -123,5 +129,10 @@ int launch_bpd_propose(const void* logits, int B, int k, int V, int dtype, bool 
 int launch_bpd_verify(const void* logits, const int32_t* proposals, int B, int k, int V, int dtype, bool vec_ok,
                       int eos, const BpdCrit& crit, int32_t* khat, int32_t* next, int* status, int num_sms,
                       cudaStream_t s);
+
+// in-run memory peaks (measurement): a vector copy, and a read-only stream (mode 0: vector
+// loads, mode 1: a bulk-copy ring into shared memory)
+int launch_peak_copy(const void* src, void* dst, int64_t bytes, int grid, cudaStream_t s);
+int launch_peak_read(const void* src, int64_t bytes, int grid, int mode, uint32_t* sink, int* status, cudaStream_t s);
 
 }  // namespace vbs
