@@ -167,8 +167,6 @@ VBS_EXPORT int bs_init(vbs_bs** out, int batch, int W, int V, int eos, double al
     a.row_one = cv.take<int>(R);
     a.row_p0 = cv.take<int>(R);
     a.row_np = cv.take<int>(R);
-    a.sent_np = cv.take<int>(batch);
-    a.sent_ticket = cv.take<int>(batch);
     a.done_count = cv.take<int>(1);
     a.all_done_dev = cv.take<int32_t>(1);
     a.status = cv.take<int>(1);
@@ -194,27 +192,14 @@ VBS_EXPORT int bs_init(vbs_bs** out, int batch, int W, int V, int eos, double al
     }
   }
   // which CTAs hold each row: row r spans elements [r V, (r + 1) V) of the flat split
-  std::vector<int> p0(R), np(R), snp(batch, 0);
+  std::vector<int> p0(R), np(R);
   for (int64_t r = 0; r < R; ++r) {
     p0[r] = static_cast<int>((r * V) / per);
     np[r] = static_cast<int>(((r + 1) * V - 1) / per - (r * V) / per + 1);
-    snp[r / W] += np[r];
   }
-  // the flat kernel: each CTA merges the sentences it completes, at most as many as its
-  // range touches
-  int64_t most = 0;
-  for (int64_t g = 0; g < G; ++g) {
-    const int64_t e0 = g * per, e1 = std::min(e0 + per, total);
-    most = std::max(most, ((e1 - 1) / V) / W - (e0 / V) / W + 1);
-  }
-  const bool flat_fits = most <= vbs::bs_flat_pend_cap();
-  a.flat = 0;                        // measured slower than the cluster and two-kernel paths so far
-  (void)flat_fits;
   bool ok = cudaMemsetAsync(c->dev_block, 0, cv.off, c->stream) == cudaSuccess;
   ok = ok && cudaMemcpyAsync(a.row_p0, p0.data(), R * sizeof(int), cudaMemcpyHostToDevice, c->stream) == cudaSuccess;
   ok = ok && cudaMemcpyAsync(a.row_np, np.data(), R * sizeof(int), cudaMemcpyHostToDevice, c->stream) == cudaSuccess;
-  ok = ok && cudaMemcpyAsync(a.sent_np, snp.data(), batch * sizeof(int), cudaMemcpyHostToDevice, c->stream) ==
-             cudaSuccess;
   const std::vector<int> ones(R, 1);
   ok = ok && cudaMemcpyAsync(a.row_one, ones.data(), R * sizeof(int), cudaMemcpyHostToDevice, c->stream) == cudaSuccess;
   ok = ok && cudaStreamSynchronize(c->stream) == cudaSuccess;

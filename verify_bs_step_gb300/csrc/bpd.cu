@@ -189,11 +189,15 @@ __global__ void __launch_bounds__(BPD_NT) bpd_verify_kernel(const void* logits, 
 constexpr int BPD_RT = 256;
 constexpr int BPD_BUF = 64 * 1024;        // shared staging of one row chunk (bulk copy)
 
-// The CTA's staging buffer and its mbarrier (one bulk copy in flight at a time).
+// The CTA's staging buffer, its pieces' mbarriers and their phases (bit p: piece p), and
+// the row maxima of the single-barrier reduction (two slots, alternating by row).
+constexpr int BPD_PIECES = 1;                      // a chunk arrives in this many bulk copies (more measured slower)
 struct RowStage {
   unsigned char* buf;
-  u64* bar;
+  u64* bar;                                        // [BPD_PIECES]
   u32 phase;
+  u64* best;                                       // [2]
+  u32 row;                                         // rows scanned so far (selects the slot)
 };
 
 __device__ __forceinline__ u32 gt_bf16x2(u32 a, u32 b) {
@@ -231,33 +235,44 @@ __device__ int row_argmax(const char* row, int V, RowStage& st, u64* red, int* s
       const int nv = min(CH, nvec - c0);
       __syncthreads();                             // the buffer's previous contents are consumed
       if (tid == 0) {
-        mbar_expect_tx(st.bar, static_cast<u32>(nv) * 16u);
-        bulk_g2s(st.buf, row + static_cast<int64_t>(c0) * 16, static_cast<u32>(nv) * 16u, st.bar);
+        if (c0 == 0 && !RANK) st.best[(st.row + 1) & 1] = 0ull;   // the next row's slot (read before this barrier)
+        for (int pc = 0; pc < BPD_PIECES; ++pc) {
+          const int lo = nv * pc / BPD_PIECES, hi = nv * (pc + 1) / BPD_PIECES;
+          if (hi == lo) continue;
+          mbar_expect_tx(&st.bar[pc], static_cast<u32>(hi - lo) * 16u);
+          bulk_g2s(st.buf + lo * 16, row + static_cast<int64_t>(c0 + lo) * 16, static_cast<u32>(hi - lo) * 16u,
+                   &st.bar[pc]);
+        }
       }
       if (RANK && c0 == 0) xp = token_value<T>(row, prop, V);   // in flight with the copy
-      if (!mbar_wait(st.bar, st.phase)) set_status(status, VBS_ETIMEOUT);
-      st.phase ^= 1u;
       const uint4* v = reinterpret_cast<const uint4*>(st.buf);
-      for (int i = tid; i < nv; i += BPD_RT) {
-        const uint4 q = v[i];
-        const float m = VecMax<T>::finish(VecMax<T>::fold(q, VecMax<T>::NEG));
-        if (m > bv || bi < 0) { bv = m; bi = c0 + i; bq = q; }
-        if constexpr (RANK) {
-          const int v0 = (c0 + i) * VEC;
-          bool tie = true;
-          if constexpr (Elem<T>::BYTES == 2) {
-            const u32 xb = __float_as_uint(xp) >> 16, refw = xb | (xb << 16);
-            cnt += static_cast<int>((__popc(gt_bf16x2(q.x, refw)) + __popc(gt_bf16x2(q.y, refw)) +
-                                     __popc(gt_bf16x2(q.z, refw)) + __popc(gt_bf16x2(q.w, refw))) >> 4);
-            tie = (eq_bf16x2(q.x, refw) | eq_bf16x2(q.y, refw) | eq_bf16x2(q.z, refw) | eq_bf16x2(q.w, refw)) != 0u;
-          }
-          if (tie) {
-            float x[VEC];
-            Vec16<T>::unpack(q, x);
+      for (int pc = 0; pc < BPD_PIECES; ++pc) {
+        const int lo = nv * pc / BPD_PIECES, hi = nv * (pc + 1) / BPD_PIECES;
+        if (hi == lo) continue;
+        // each piece is scanned as soon as it lands, while the later ones are still in flight
+        if (!mbar_wait(&st.bar[pc], (st.phase >> pc) & 1u)) set_status(status, VBS_ETIMEOUT);
+        st.phase ^= 1u << pc;
+        for (int i = lo + tid; i < hi; i += BPD_RT) {
+          const uint4 q = v[i];
+          const float m = VecMax<T>::finish(VecMax<T>::fold(q, VecMax<T>::NEG));
+          if (m > bv || bi < 0) { bv = m; bi = c0 + i; bq = q; }
+          if constexpr (RANK) {
+            const int v0 = (c0 + i) * VEC;
+            bool tie = true;
+            if constexpr (Elem<T>::BYTES == 2) {
+              const u32 xb = __float_as_uint(xp) >> 16, refw = xb | (xb << 16);
+              cnt += static_cast<int>((__popc(gt_bf16x2(q.x, refw)) + __popc(gt_bf16x2(q.y, refw)) +
+                                       __popc(gt_bf16x2(q.z, refw)) + __popc(gt_bf16x2(q.w, refw))) >> 4);
+              tie = (eq_bf16x2(q.x, refw) | eq_bf16x2(q.y, refw) | eq_bf16x2(q.z, refw) | eq_bf16x2(q.w, refw)) != 0u;
+            }
+            if (tie) {
+              float x[VEC];
+              Vec16<T>::unpack(q, x);
 #pragma unroll
-            for (int e2 = 0; e2 < VEC; ++e2) {
-              if constexpr (Elem<T>::BYTES == 2) cnt += (x[e2] == xp && v0 + e2 < prop) ? 1 : 0;
-              else cnt += beats(x[e2], v0 + e2, xp, prop);
+              for (int e2 = 0; e2 < VEC; ++e2) {
+                if constexpr (Elem<T>::BYTES == 2) cnt += (x[e2] == xp && v0 + e2 < prop) ? 1 : 0;
+                else cnt += beats(x[e2], v0 + e2, xp, prop);
+              }
             }
           }
         }
@@ -281,6 +296,18 @@ __device__ int row_argmax(const char* row, int V, RowStage& st, u64* red, int* s
     }
   }
   best = warp_max_u64(best);
+  if constexpr (!RANK) {
+    if (VECTOR) {
+      // one barrier: the warps' maxima meet in this row's slot, which thread 0 cleared before
+      // the previous row's first barrier
+      u64* slot = &st.best[st.row & 1];
+      if (lane == 0) atomicMax(slot, best);
+      __syncthreads();
+      const u64 v = *reinterpret_cast<volatile u64*>(slot);
+      st.row += 1;
+      return static_cast<int>(key_v(v));
+    }
+  }
   if constexpr (RANK) cnt = __reduce_add_sync(FULL, cnt);
   if (lane == 0) {
     red[warp] = best;
@@ -345,25 +372,31 @@ __global__ void __launch_bounds__(BPD_RT, 3) bpd_verify_queue_kernel(const void*
   extern __shared__ __align__(128) unsigned char bpd_smem[];
   __shared__ u64 red[BPD_RT / 32 + 1];
   __shared__ int redc[BPD_RT / 32 + 1];
-  __shared__ __align__(8) u64 bar;
+  __shared__ __align__(8) u64 bar[BPD_PIECES];
+  __shared__ __align__(8) u64 best2[2];
   __shared__ int s_unit, s_b, s_h, s_q;
   const int tid = threadIdx.x;
   if (tid == 0) {
-    mbar_init(&bar, 1);
+    for (int pc = 0; pc < BPD_PIECES; ++pc) mbar_init(&bar[pc], 1);
     fence_mbar_init();
+    best2[0] = 0ull;
+    best2[1] = 0ull;
   }
   __syncthreads();
-  RowStage st{bpd_smem, &bar, 0u};
-  const u64 tag = static_cast<u64>(*reinterpret_cast<volatile unsigned*>(&g_bpd_epoch) + 1u) << 32;
+  RowStage st{bpd_smem, bar, 0u, best2, 0u};
+  u64 tag = 0;                                     // this call's ready-list tag, read when first needed
   const int64_t row_bytes = static_cast<int64_t>(V) * Elem<T>::BYTES;
   const int n_rows = B * (k - 1);
-  // chains
+  // chains: CTA i starts with chain i, the rest are handed out by the counter (offset by the
+  // grid); each CTA asks for its next chain while it runs the current one
+  int next_b = static_cast<int>(blockIdx.x);
   for (;;) {
-    if (tid == 0) s_unit = atomicAdd(&g_bpd_next_chain, 1);
+    if (tid == 0) s_unit = next_b;
     __syncthreads();
     const int b = s_unit;
     __syncthreads();
     if (b >= B) break;
+    if (tid == 0) next_b = static_cast<int>(gridDim.x) + atomicAdd(&g_bpd_next_chain, 1);
     const char* base = reinterpret_cast<const char*>(logits) + static_cast<int64_t>(b) * k * k * row_bytes;
     const int32_t* props = proposals + static_cast<int64_t>(b) * k;
     int checks = k - 1;                            // proposals up to an EOS need no checks past it
@@ -373,9 +406,6 @@ __global__ void __launch_bounds__(BPD_RT, 3) bpd_verify_queue_kernel(const void*
     int n = 1, am = -1, last = -1;
     for (int p = 0; p < checks; ++p) {
       const char* row = base + static_cast<int64_t>(p) * k * row_bytes;
-      // the next head-0 row is read unless this check fails: start it towards L2
-      if (VECTOR && tid == 0 && p + 1 <= checks)
-        prefetch_row_l2(base + static_cast<int64_t>(p + 1) * k * row_bytes, row_bytes);
       const int prop = __ldg(props + p + 1);
       int rank = 0;
       if constexpr (RANK) {
@@ -400,6 +430,7 @@ __global__ void __launch_bounds__(BPD_RT, 3) bpd_verify_queue_kernel(const void*
       khat_out[b] = n;
       next_out[static_cast<int64_t>(b) * k] = am;
       if (k > 1) {
+        if (!tag) tag = static_cast<u64>(*reinterpret_cast<volatile unsigned*>(&g_bpd_epoch) + 1u) << 32;
         const int slot = atomicAdd(&g_bpd_ready_tail, k - 1);
         for (int h = 1; h < k; ++h)
           st_release_u64(&g_bpd_ready[slot + h - 1], tag | (static_cast<u64>(b) << 5) | static_cast<u64>(h));
@@ -407,6 +438,7 @@ __global__ void __launch_bounds__(BPD_RT, 3) bpd_verify_queue_kernel(const void*
     }
   }
   // published rows: head h at position khat_b - 1
+  if (tid == 0 && !tag) tag = static_cast<u64>(*reinterpret_cast<volatile unsigned*>(&g_bpd_epoch) + 1u) << 32;
   for (;;) {
     if (tid == 0) {
       const int r = atomicAdd(&g_bpd_ready_head, 1);
@@ -432,9 +464,9 @@ __global__ void __launch_bounds__(BPD_RT, 3) bpd_verify_queue_kernel(const void*
     const int am = row_argmax<T, VECTOR>(row, V, st, red, status);
     if (tid == 0) next_out[static_cast<int64_t>(b) * k + h] = am;
   }
-  // the last CTA out resets the queue and moves the ready list to the next epoch
+  // the last CTA out resets the queue and moves the ready list to the next epoch (the next
+  // call on the stream starts once this grid has completed)
   if (tid == 0) {
-    __threadfence();
     if (atomicAdd(&g_bpd_exited, 1) == static_cast<int>(gridDim.x) - 1) {
       g_bpd_next_chain = 0;
       g_bpd_ready_head = 0;

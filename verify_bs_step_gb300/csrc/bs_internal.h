@@ -65,9 +65,6 @@ struct BsArgs {
   int* row_np;                    // [R] the number of CTAs (partials) holding row r
   int* done_count;                // sentences finished (step-local counter)
   int cluster;                    // 0: flat split + merge kernel; C: a cluster of C CTAs per sentence
-  int flat;                       // 1: bs_step runs the flat kernel (merges by per-sentence tickets)
-  int* sent_np;                   // [B] row segments of sentence b in the flat split (tickets per step)
-  int* sent_ticket;               // [B] segments published this step (reset by the merging CTA)
   int* done;
   // finished sets
   double* fin_ns;
@@ -97,7 +94,6 @@ int launch_bs_finalize(const BsArgs& a, const float* scores, const int32_t* seqs
                        int32_t* out_len, float* out_score, cudaStream_t s);
 constexpr int BS_NSLOT = 4;       // row segments one stream CTA holds (cluster mode: W / C <= this)
 int bs_threads_per_cta();
-int bs_flat_pend_cap();           // sentences one flat-kernel CTA can merge
 int bs_ctas_per_sm();
 
 // bs_expand_static: scratch in a static device array of this size; rows at most.  With

@@ -1180,9 +1180,9 @@ __device__ int merge_load_state(const BsArgs& a, MergeShared& sm, int b) {
   return done_b;
 }
 
-// Threads 0..NT-1 (NT a multiple of 32, at least 2W... one warp per row at a time): sentence
-// b's merge once its state and partials are in shared memory (the caller's barrier has
-// passed): row LSEs and lists, the ranking by (score desc, flat index asc), the walk with
+// Threads 0..NT-1 (NT a multiple of 32; the warps take the rows in turn): sentence b's merge
+// once its state and partials are in shared memory (the caller's barrier has passed): row
+// LSEs and lists, the ranking by (score desc, flat index asc), the walk with
 // BeamHypotheses.add, the stopping test, the outputs and the in-place sequence gather.
 template <int NT, int BAR>
 __device__ void merge_sentence(const BsArgs& a, MergeShared& sm, int b, int done_b) {
@@ -1362,533 +1362,6 @@ __global__ void __launch_bounds__(MG_NT) bs_merge_kernel(const BsArgs a) {
   merge_prefetch_partials(a, sm, b, MG_NT);
   __syncthreads();
   merge_sentence<MG_NT, 0>(a, sm, b, done_b);
-}
-
-// ---------------------------------------------------------------------------------------
-// the flat kernel: every SM streams, sentences merge where their last segment lands
-// ---------------------------------------------------------------------------------------
-//
-// One CTA per SM over equal ranges of the flattened [R, V] space (the stream kernel's
-// split).  A row segment is resolved by the last consumer warp to leave it while the
-// others stream on; that warp writes the segment's partial (max, scaled sum, K best keys)
-// to global memory and takes a ticket of the segment's sentence.  The CTA whose ticket
-// completes a sentence merges it after its own range (every consumer warp, one load
-// round for the partials, the state and the first sequence tile).  A segment whose queue
-// overflowed is rescanned by all consumer warps after the loop.  No CTA waits for
-// another; every wait inside a CTA is bounded.
-
-constexpr int PEND_CAP = 32;                       // sentences one CTA may merge
-constexpr int DEF_CAP = 4;                         // segments one CTA defers to a CTA-wide rescan
-constexpr int RS_CAP = 2048;                       // keys a CTA-wide rescan collects per pass
-
-struct FlatDeferred {
-  int r, v0, v1, pslot;
-  u32 bar;
-  float M, l;
-};
-
-struct FlatShared {
-  unsigned char ring[NSTAGE][STAGE_BYTES];     // the streamed chunks; after the loop, rescans and merges
-  u64 q[NSLOT][QSEG];
-  u32 qd[NSLOT][QSEG];
-  u64 fin[NSLOT][FIN_CAP];
-  u32 ctile[NSLOT][CT_CAP];
-  float M[NSLOT][BS_NCW], l[NSLOT][BS_NCW];
-  u64 full[NSTAGE], empty[NSTAGE];
-  u32 thr[NSLOT], sbar[NSLOT], tmin[NSLOT];
-  int qcnt[NSLOT], qref[NSLOT], fcnt[NSLOT], mode[NSLOT];
-  int seg_r[NSLOT], seg_v0[NSLOT], seg_v1[NSLOT], seg_skip[NSLOT];
-  int seg_arrive[NSLOT];                       // consumer warps done with the slot's segment
-  int slot_gen[NSLOT];                         // segments published from the slot
-  int stage_skip[NSTAGE];
-  int pend[PEND_CAP];                          // sentences this CTA completed
-  int npend;
-  FlatDeferred dfr[DEF_CAP];
-  int ndfr;
-  int rcnt;
-  u64 rbar;
-};
-
-static_assert(sizeof(FlatShared) <= 232448, "the flat kernel's shared memory fits one SM");
-static_assert(sizeof(MergeShared) + (RS_CAP + KMAX) * 8 <= sizeof(FlatShared::ring), "the merge fits the ring");
-
-// The producer of the stream kernel, on the flat kernel's shared layout.
-template <typename T, class SH>
-__device__ void produce_ring(const BsArgs& a, SH& sh, int64_t e0, int64_t e1) {
-  constexpr int VEC = Vec16<T>::N;
-  constexpr int64_t SE = static_cast<int64_t>(BS_NC) * BS_U * VEC;
-  bool skip = false;
-  ChunkCursor cur(e0, e1, a.V, static_cast<int>(SE));
-  for (int c = 0; cur.more(); ++c) {
-    const Chunk ch = cur.next();
-    if (ch.first) skip = row_skipped(a, ch.r);
-    const int slot = c % NSTAGE;
-    if (c >= NSTAGE && !mbar_wait(&sh.empty[slot], static_cast<u32>(((c / NSTAGE) + 1) & 1)))
-      set_status(a.status, VBS_ETIMEOUT);
-    const u32 bytes = skip ? 0u : static_cast<u32>(ch.len * Elem<T>::BYTES);
-    sh.stage_skip[slot] = skip ? 1 : 0;
-    mbar_expect_tx(&sh.full[slot], bytes);
-    if (bytes) {
-      const char* src = reinterpret_cast<const char*>(a.logits) +
-                        (static_cast<int64_t>(ch.r) * a.ld + ch.v0) * Elem<T>::BYTES;
-      bulk_g2s(sh.ring[slot], src, bytes, &sh.full[slot]);
-    }
-  }
-}
-
-// One lane: the segment's ticket; the CTA that completes the sentence merges it later.
-__device__ __forceinline__ void flat_ticket(const BsArgs& a, FlatShared& sh, int r) {
-  const int b = r / a.W;
-  __threadfence();                                  // the partial is visible before the ticket
-  const int old = atomicAdd(a.sent_ticket + b, 1);
-  if (old == a.sent_np[b] - 1) {
-    __threadfence();                                // and the others' partials before the merge
-    const int p = atomicAdd(&sh.npend, 1);
-    if (p < PEND_CAP) sh.pend[p] = b;
-    else set_status(a.status, VBS_ESTATE);
-  }
-}
-
-// One warp: write segment s's K best keys (sorted, from fin) and its (max, scaled sum).
-__device__ void flat_write_partial(const BsArgs& a, FlatShared& sh, int s, float Mw, float lw, int lane) {
-  const int K = a.K;
-  const int r = sh.seg_r[s];
-  const int64_t pslot = static_cast<int64_t>(r) * a.P + (static_cast<int>(blockIdx.x) - a.row_p0[r]);
-  u64* out = a.part_key + pslot * K;
-  const int cnt = sh.fcnt[s];
-  for (int j = lane; j < cnt; j += 32) {
-    const u64 k = sh.fin[s][j];
-    int rank = 0;
-    for (int i = 0; i < cnt; ++i) rank += sh.fin[s][i] > k;
-    if (rank < K) out[rank] = k;
-  }
-  if (lane < K && lane >= cnt) out[lane] = 0ull;
-  if (lane == 0) {
-    a.part_M[pslot] = Mw;
-    a.part_l[pslot] = lw;
-  }
-}
-
-// One warp, keys of a segment collected alone (a deferred rescan did not fit): every key
-// at or above a rising bar, from global memory, QSEG at a time, into q[s].
-template <typename T, int VEC>
-__device__ void flat_warp_rescan(const BsArgs& a, FlatShared& sh, int s, int lane) {
-  const int K = a.K;
-  const int r = sh.seg_r[s], sv0 = sh.seg_v0[s], sv1 = sh.seg_v1[s];
-  const char* row = reinterpret_cast<const char*>(a.logits) + static_cast<int64_t>(r) * a.ld * Elem<T>::BYTES;
-  u64 bar = static_cast<u64>(sh.sbar[s]) << 32;
-  for (;;) {
-    for (int i = lane; i < QSEG; i += 32) sh.q[s][i] = 0ull;
-    if (lane == 0) sh.qcnt[s] = 0;
-    __syncwarp();
-    for (int v = sv0 + lane * VEC; v < sv1; v += 32 * VEC) {
-      float x[VEC];
-      if constexpr (VEC == 1) x[0] = Elem<T>::load(row, v);
-      else Vec16<T>::unpack(ld_stream16(row + static_cast<int64_t>(v) * Elem<T>::BYTES), x);
-#pragma unroll
-      for (int e2 = 0; e2 < VEC; ++e2) {
-        const u64 k = make_key(x[e2], static_cast<u32>(v + e2));
-        if (k >= bar) {
-          const int pos = atomicAdd(&sh.qcnt[s], 1);
-          if (pos < QSEG) sh.q[s][pos] = k;
-        }
-      }
-    }
-    __syncwarp();
-    const int n = sh.qcnt[s];
-    __syncwarp();
-    if (n <= QSEG) break;
-    warp_select_topk(sh.q[s], QSEG, K, sh.fin[s], lane);
-    bar = sh.fin[s][K - 1];
-  }
-  warp_select_topk(sh.q[s], sh.qcnt[s], K, sh.fin[s], lane);
-  if (lane == 0) sh.fcnt[s] = min(sh.qcnt[s], K);
-  __syncwarp();
-}
-
-// One warp (the last to leave segment s): resolve, publish or defer, take the ticket,
-// clear the slot and hand it back.
-template <typename T, int VEC, bool BIGK>
-__device__ void flat_publish(const BsArgs& a, FlatShared& sh, int s, int lane) {
-  const bool skip = sh.seg_skip[s] != 0;
-  const int r = sh.seg_r[s];
-  bool ticket = true;
-  if (!skip) {
-    float Mw = lane < BS_NCW ? sh.M[s][lane] : -INFINITY;
-    float lw = lane < BS_NCW ? sh.l[s][lane] : 0.f;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float M2 = __shfl_xor_sync(FULL, Mw, off);
-      const float l2 = __shfl_xor_sync(FULL, lw, off);
-      lse_merge(Mw, lw, M2, l2);
-    }
-    resolve_tiles<T, VEC, BIGK>(a, sh, s, lane);
-    __syncwarp();
-    if (sh.mode[s] == 1) {
-      int d = 0;
-      if (lane == 0) d = atomicAdd(&sh.ndfr, 1);
-      d = __shfl_sync(FULL, d, 0);
-      if (d < DEF_CAP) {
-        if (lane == 0) {
-          FlatDeferred& f = sh.dfr[d];
-          f.r = r;
-          f.v0 = sh.seg_v0[s];
-          f.v1 = sh.seg_v1[s];
-          f.pslot = r * a.P + (static_cast<int>(blockIdx.x) - a.row_p0[r]);
-          f.bar = sh.sbar[s];
-          f.M = Mw;
-          f.l = lw;
-        }
-        ticket = false;                             // taken after the CTA-wide rescan
-      } else {
-        flat_warp_rescan<T, VEC>(a, sh, s, lane);
-      }
-    }
-    if (ticket) flat_write_partial(a, sh, s, Mw, lw, lane);
-  }
-  __syncwarp();
-  if (ticket && lane == 0) flat_ticket(a, sh, r);
-  // clear the slot for the segment NSLOT later
-  const int n = min(sh.qcnt[s], QSEG);
-  for (int j = lane; j < n; j += 32) sh.q[s][j] = 0ull;
-  __syncwarp();
-  if (lane == 0) {
-    sh.qcnt[s] = 0;
-    sh.qref[s] = 0;
-    sh.thr[s] = 0u;
-    sh.tmin[s] = 0xffffffffu;
-    sh.mode[s] = 0;
-    sh.seg_arrive[s] = 0;
-    __threadfence_block();
-    atomicAdd(&sh.slot_gen[s], 1);
-  }
-}
-
-// The consumers of the flat kernel: the stream kernel's loop, except that a row segment is
-// published by the last warp to leave it and a slot is reused once that is done.  SEED:
-// the warps meet at each segment's first chunk to start from the best of their seeds.
-template <typename T, bool TMA, bool BIGK, bool SEED>
-__device__ void flat_consume(const BsArgs& a, FlatShared& sh, int64_t e0, int64_t e1) {
-  constexpr int VEC = TMA ? Vec16<T>::N : 1;
-  constexpr int64_t SE = static_cast<int64_t>(BS_NC) * BS_U * VEC;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int K = a.K;
-  float M = -INFINITY, m = -INFINITY, l = 0.f;
-  bool skip = false, seeded = false;
-  int seg = -1, slot = 0;
-  ChunkCursor cur(e0, e1, a.V, static_cast<int>(SE));
-  for (int c = 0; cur.more(); ++c) {
-    const Chunk ch = cur.next();
-    if (ch.first) {
-      ++seg;
-      slot = seg % NSLOT;
-      const int gen = seg / NSLOT;
-      if (gen > 0) {                                // the slot's previous segment must be published
-        if (lane == 0) {
-          u32 it = 0;
-          while (*reinterpret_cast<volatile int*>(&sh.slot_gen[slot]) < gen) {
-            if (++it > (1u << 24)) { set_status(a.status, VBS_ETIMEOUT); break; }
-          }
-          __threadfence_block();
-        }
-        __syncwarp();
-      }
-      if constexpr (!TMA) skip = row_skipped(a, ch.r);
-      M = -INFINITY;
-      m = -INFINITY;
-      l = 0.f;
-      seeded = false;
-    }
-    const int n = ch.len / VEC;
-    uint4 q[BS_U];
-    float xs[BS_U];
-    if constexpr (TMA) {
-      const int rs = c % NSTAGE;
-      if (!mbar_wait(&sh.full[rs], static_cast<u32>((c / NSTAGE) & 1))) set_status(a.status, VBS_ETIMEOUT);
-      skip = sh.stage_skip[rs] != 0;
-#pragma unroll
-      for (int u = 0; u < BS_U; ++u) {
-        const int i = tid + u * BS_NC;
-        constexpr u32 NEG = VecMax<T>::NEG;
-        q[u] = (!skip && i < n) ? *reinterpret_cast<const uint4*>(sh.ring[rs] + i * 16) : make_uint4(NEG, NEG, NEG, NEG);
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.empty[rs]);
-    } else {
-      const char* row = reinterpret_cast<const char*>(a.logits) +
-                        (static_cast<int64_t>(ch.r) * a.ld + ch.v0) * Elem<T>::BYTES;
-#pragma unroll
-      for (int u = 0; u < BS_U; ++u) {
-        const int i = tid + u * BS_NC;
-        xs[u] = (!skip && i < n) ? Elem<T>::load(row, i) : -INFINITY;
-      }
-    }
-    if (ch.first && tid == 0) {
-      sh.seg_r[slot] = ch.r;
-      sh.seg_v0[slot] = ch.v0;
-      sh.seg_skip[slot] = skip ? 1 : 0;
-    }
-    if (!skip) {
-      float tm;
-      if constexpr (TMA) {
-        u32 acc = VecMax<T>::NEG;
-#pragma unroll
-        for (int u = 0; u < BS_U; ++u) acc = VecMax<T>::fold(q[u], acc);
-        tm = VecMax<T>::finish(acc);
-      } else {
-        tm = xs[0];
-#pragma unroll
-        for (int u = 1; u < BS_U; ++u) tm = fmaxf(tm, xs[u]);
-      }
-      u32 thr_o = *reinterpret_cast<volatile u32*>(&sh.thr[slot]);
-      const u32 tmo = tm > -INFINITY ? ord_f32(tm) : 0u;
-      if (!seeded) {
-        seeded = true;
-        const u32 seed = warp_kth_u32(tmo, K, lane);
-        if (lane == 0 && seed > thr_o) atomicMax(&sh.thr[slot], seed);
-        thr_o = seed > thr_o ? seed : thr_o;
-        if constexpr (BIGK) {
-          const u32 seed_j = warp_kth_u32(tmo, (K + BS_NCW - 1) / BS_NCW, lane);
-          if (lane == 0) atomicMin(&sh.tmin[slot], seed_j);
-        }
-        if constexpr (SEED) {
-          named_sync(BAR_CONSUMERS, BS_NC);
-          thr_o = *reinterpret_cast<volatile u32*>(&sh.thr[slot]);
-          if constexpr (BIGK) {
-            const u32 mn = *reinterpret_cast<volatile u32*>(&sh.tmin[slot]);
-            if (mn > thr_o) {
-              thr_o = mn;
-              if (lane == 0) atomicMax(&sh.thr[slot], mn);
-            }
-          }
-        }
-      }
-      if (tmo != 0u && tmo >= thr_o) {
-        int um = -1, em = -1;
-        float sec = -INFINITY;
-        uint4 qm = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-        for (int u = 0; u < BS_U; ++u) {
-          float vmu;
-          if constexpr (TMA) vmu = VecMax<T>::finish(VecMax<T>::fold(q[u], VecMax<T>::NEG));
-          else vmu = xs[u];
-          const bool hit = um < 0 && vmu == tm;
-          if (hit) {
-            um = u;
-            if constexpr (TMA) qm = q[u];
-            else qm.x = __float_as_uint(xs[u]);
-          } else {
-            sec = fmaxf(sec, vmu);
-          }
-        }
-        float x[VEC];
-        if constexpr (TMA) Vec16<T>::unpack(qm, x);
-        else x[0] = __uint_as_float(qm.x);
-#pragma unroll
-        for (int e2 = 0; e2 < VEC; ++e2) {
-          const bool hit = em < 0 && x[e2] == tm;
-          if (hit) em = e2;
-          else sec = fmaxf(sec, x[e2]);
-        }
-        const u32 so = sec > -INFINITY ? ord_f32(sec) : 0u;
-        const bool known = um >= 0 && em >= 0 && tm != 0.0f && sec != 0.0f && so < 0xffffffe0u;
-        const u32 desc = known ? (((so >> 5) + 1u) << 5) | static_cast<u32>(um * VEC + em) : 0xffffffffu;
-        const int pos = atomicAdd(&sh.qcnt[slot], 1);
-        if (pos < QSEG) {
-          sh.q[slot][pos] = (static_cast<u64>(tmo) << 32) | static_cast<u32>(ch.v0 + tid * VEC);
-          sh.qd[slot][pos] = desc;
-        }
-      }
-      if (tm > m) {
-        const float Mn = tm * LOG2E_F;
-        l *= ex2(M - Mn);
-        M = Mn;
-        m = tm;
-      }
-      if (tm > -INFINITY) {
-        float acc[BS_U];
-#pragma unroll
-        for (int u = 0; u < BS_U; ++u) {
-          float x[VEC];
-          if constexpr (TMA) Vec16<T>::unpack(q[u], x);
-          else x[0] = xs[u];
-#pragma unroll
-          for (int e2 = 0; e2 < VEC; ++e2) x[e2] = ex2(fmaf(x[e2], LOG2E_F, -M));
-#pragma unroll
-          for (int w = 1; w < VEC; w <<= 1)
-#pragma unroll
-            for (int e2 = 0; e2 + w < VEC; e2 += 2 * w) x[e2] += x[e2 + w];
-          acc[u] = x[0];
-        }
-#pragma unroll
-        for (int w = 1; w < BS_U; w <<= 1)
-#pragma unroll
-          for (int u = 0; u + w < BS_U; u += 2 * w) acc[u] += acc[u + w];
-        l += acc[0];
-      }
-      if (warp == (c & (BS_NCW - 1))) {
-        const int nq = __shfl_sync(FULL, *reinterpret_cast<volatile int*>(&sh.qcnt[slot]), 0);
-        const int nr = __shfl_sync(FULL, *reinterpret_cast<volatile int*>(&sh.qref[slot]), 0);
-        if (nq >= nr + QSTEP) queue_refresh<BIGK>(sh, slot, nq < QSEG ? nq : QSEG, K, lane);
-      }
-    }
-    if (ch.last) {
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float M2 = __shfl_xor_sync(FULL, M, off);
-        const float l2 = __shfl_xor_sync(FULL, l, off);
-        lse_merge(M, l, M2, l2);
-      }
-      if (lane == 0) { sh.M[slot][warp] = M; sh.l[slot][warp] = l; }
-      if (tid == 0) sh.seg_v1[slot] = ch.v0 + ch.len;
-      __syncwarp();
-      int old = 0;
-      if (lane == 0) {
-        __threadfence_block();
-        old = atomicAdd(&sh.seg_arrive[slot], 1);
-        __threadfence_block();
-      }
-      old = __shfl_sync(FULL, old, 0);
-      __syncwarp();
-      if (old == BS_NCW - 1) flat_publish<T, VEC, BIGK>(a, sh, slot, lane);
-    }
-  }
-}
-
-// All consumer threads, after the loop: the deferred segments, each rescanned CTA-wide from
-// its final bar, written and ticketed.
-template <typename T, int VEC>
-__device__ void flat_rescans(const BsArgs& a, FlatShared& sh) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int K = a.K;
-  u64* buf = reinterpret_cast<u64*>(&sh.ring[0][0]);
-  u64* sel = buf + RS_CAP;
-  const int nd = min(sh.ndfr, DEF_CAP);
-  for (int d = 0; d < nd; ++d) {
-    const FlatDeferred f = sh.dfr[d];
-    const char* row = reinterpret_cast<const char*>(a.logits) + static_cast<int64_t>(f.r) * a.ld * Elem<T>::BYTES;
-    if (tid == 0) sh.rbar = static_cast<u64>(f.bar) << 32;
-    for (;;) {
-      named_sync(BAR_CONSUMERS, BS_NC);
-      const u64 bar = sh.rbar;
-      if (tid == 0) sh.rcnt = 0;
-      named_sync(BAR_CONSUMERS, BS_NC);
-      for (int v = f.v0 + tid * VEC; v < f.v1; v += BS_NC * VEC) {
-        float x[VEC];
-        if constexpr (VEC == 1) x[0] = Elem<T>::load(row, v);
-        else Vec16<T>::unpack(ld_stream16(row + static_cast<int64_t>(v) * Elem<T>::BYTES), x);
-#pragma unroll
-        for (int e2 = 0; e2 < VEC; ++e2) {
-          const u64 k = make_key(x[e2], static_cast<u32>(v + e2));
-          if (k >= bar) {
-            const int pos = atomicAdd(&sh.rcnt, 1);
-            if (pos < RS_CAP) buf[pos] = k;
-          }
-        }
-      }
-      named_sync(BAR_CONSUMERS, BS_NC);
-      const int n = sh.rcnt;
-      named_sync(BAR_CONSUMERS, BS_NC);
-      if (n <= RS_CAP) break;
-      if (warp == 0) {
-        warp_select_topk(buf, RS_CAP, K, sel, lane);
-        if (lane == 0) sh.rbar = sel[K - 1];
-      }
-    }
-    if (warp == 0) {
-      const int n = sh.rcnt;
-      warp_select_topk(buf, n, K, sel, lane);
-      u64* out = a.part_key + static_cast<int64_t>(f.pslot) * K;
-      if (lane < K) out[lane] = lane < n ? sel[lane] : 0ull;
-      if (lane == 0) {
-        a.part_M[f.pslot] = f.M;
-        a.part_l[f.pslot] = f.l;
-      }
-      __syncwarp();
-      if (lane == 0) flat_ticket(a, sh, f.r);
-    }
-  }
-}
-
-template <typename T, bool TMA, bool BIGK, bool SEED>
-__global__ void __launch_bounds__(BS_NT, 1) bs_flat_kernel(const BsArgs a) {
-  extern __shared__ __align__(128) unsigned char bs_smem[];
-  FlatShared& sh = *reinterpret_cast<FlatShared*>(bs_smem);
-  const int64_t total = static_cast<int64_t>(a.R) * a.V;
-  const int64_t e0 = static_cast<int64_t>(blockIdx.x) * a.per;
-  const int64_t e1 = min(e0 + a.per, total);
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < NSTAGE; ++s) {
-      mbar_init(&sh.full[s], 1);
-      mbar_init(&sh.empty[s], BS_NCW);
-    }
-    fence_mbar_init();
-    sh.npend = 0;
-    sh.ndfr = 0;
-  }
-  if (threadIdx.x < NSLOT) {
-    sh.thr[threadIdx.x] = 0u;
-    sh.tmin[threadIdx.x] = 0xffffffffu;
-    sh.qcnt[threadIdx.x] = 0;
-    sh.qref[threadIdx.x] = 0;
-    sh.mode[threadIdx.x] = 0;
-    sh.seg_arrive[threadIdx.x] = 0;
-    sh.slot_gen[threadIdx.x] = 0;
-  }
-  for (int i = threadIdx.x; i < NSLOT * QSEG; i += BS_NT) (&sh.q[0][0])[i] = 0ull;
-  __syncthreads();
-  // launched as a programmatic dependent: the set-up above overlaps the previous kernel's
-  // tail; every global access comes after it has completed
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if ((threadIdx.x >> 5) == BS_NCW) {
-    if (TMA && (threadIdx.x & 31) == 0 && e0 < e1) produce_ring<T>(a, sh, e0, e1);
-    return;
-  }
-  constexpr int VEC = TMA ? Vec16<T>::N : 1;
-  if (e0 < e1) flat_consume<T, TMA, BIGK, SEED>(a, sh, e0, e1);
-  named_sync(BAR_CONSUMERS, BS_NC);
-  if (sh.ndfr > 0) {                              // (past DEF_CAP, a segment was rescanned by its warp)
-    flat_rescans<T, VEC>(a, sh);
-    named_sync(BAR_CONSUMERS, BS_NC);
-  }
-  // the sentences this CTA completed
-  MergeShared& sm = *reinterpret_cast<MergeShared*>(&sh.ring[0][0]);
-  const int np = min(sh.npend, PEND_CAP);
-  for (int i = 0; i < np; ++i) {
-    const int b = sh.pend[i];
-    const int done_b = merge_load_state<BS_NC>(a, sm, b);
-    merge_prefetch_partials(a, sm, b, BS_NC);
-    named_sync(BAR_CONSUMERS, BS_NC);
-    merge_sentence<BS_NC, BAR_CONSUMERS>(a, sm, b, done_b);
-    if (threadIdx.x == 0) a.sent_ticket[b] = 0;    // for the next step
-    named_sync(BAR_CONSUMERS, BS_NC);
-  }
-}
-
-template <typename T, bool TMA, bool BIGK, bool SEED>
-static int launch_flat_k(const BsArgs& a, int grid, cudaStream_t s) {
-  static std::atomic<unsigned long long> attr_done{0};
-  const int smem = static_cast<int>(sizeof(FlatShared));
-  if (!smem_attr_once(bs_flat_kernel<T, TMA, BIGK, SEED>, smem, attr_done)) return VBS_ECUDA;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(BS_NT);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, bs_flat_kernel<T, TMA, BIGK, SEED>, a) == cudaSuccess ? VBS_OK : VBS_ECUDA;
-}
-
-// K > 8 keeps the warps' meeting at each segment's first chunk (its cross-warp seed needs
-// every warp); K <= 8 seeds each warp from its own lanes and never stops the others.
-template <typename T, bool TMA>
-static int launch_flat(const BsArgs& a, int grid, cudaStream_t s) {
-  return a.K > 8 ? launch_flat_k<T, TMA, true, true>(a, grid, s) : launch_flat_k<T, TMA, false, false>(a, grid, s);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -2163,7 +1636,6 @@ __global__ void __launch_bounds__(RT_NT) rtopk_pass2_kernel(const BsArgs a) {
   const char* row = reinterpret_cast<const char*>(a.logits) + static_cast<int64_t>(r) * a.ld * Elem<T>::BYTES;
   const int n = a.V / VEC;
   if (tid == 0) bar = static_cast<u64>(a.rtopk_bar[r]) << 32;
-  int c = 0;                                        // the last pass's count, read by every thread
   for (;;) {
     if (tid == 0) cnt = 0;
     __syncthreads();
@@ -2192,8 +1664,9 @@ __global__ void __launch_bounds__(RT_NT) rtopk_pass2_kernel(const BsArgs a) {
         }
       }
     }
+    __threadfence_block();
     __syncthreads();
-    c = cnt;
+    const int c = cnt;
     __syncthreads();                                // every thread has read the count
     if (c <= RT_CAP) break;                         // the same for every thread
     if (warp == 0) {
@@ -2202,8 +1675,11 @@ __global__ void __launch_bounds__(RT_NT) rtopk_pass2_kernel(const BsArgs a) {
     }
     __syncthreads();
   }
+  // the count is read again here, after the second barrier: a selection over the count read
+  // right after the collection barrier was seen, in two builds, to miss one key a lane of
+  // warp 0 had queued; with the count read here no miss has been seen
   if (warp == 0) {
-    warp_select_topk(q, c, K, sel, lane);
+    warp_select_topk(q, min(*reinterpret_cast<volatile int*>(&cnt), RT_CAP), K, sel, lane);
     if (lane < K) a.part_key[static_cast<int64_t>(r) * a.P * K + lane] = sel[lane];
   }
 }
@@ -2306,11 +1782,6 @@ int launch_bs_merge_shards(const BsArgs& a0, int n_shards, const void* partials,
 }
 
 int launch_bs_step(const BsArgs& a, int grid, bool vector_ok, cudaStream_t s) {
-  if (a.flat && !a.kv_fuse) {
-    if (a.dtype == VBS_BF16)
-      return vector_ok ? launch_flat<bf16_t, true>(a, grid, s) : launch_flat<bf16_t, false>(a, grid, s);
-    return vector_ok ? launch_flat<float, true>(a, grid, s) : launch_flat<float, false>(a, grid, s);
-  }
   if (a.cluster) {
     if (a.kv_fuse) {
       if (a.dtype == VBS_BF16)
@@ -2344,7 +1815,6 @@ int launch_bs_finalize(const BsArgs& a, const float* scores, const int32_t* seqs
 }
 
 int bs_threads_per_cta() { return BS_NT; }
-int bs_flat_pend_cap() { return PEND_CAP; }
 int bs_ctas_per_sm() { return 1; }
 
 // ---------------------------------------------------------------------------------------

@@ -46,10 +46,41 @@ __device__ void paged_remap_sentence(const PagedArgs& a, int b, const int32_t* b
 
   // one round of loads: everything the sentence's remap reads (a finished sentence's
   // state is read and left as it is); each of the first W threads checks its row's parent
+  // every load is issued before the first one is used: registers first, then shared memory
+  constexpr int LU = 4;                                   // entries per thread per round
+  const int nt = W * MB;
+  const int32_t* tab = a.table + static_cast<int64_t>(r0) * MB;
+  const int32_t* rcg = a.refcnt + static_cast<int64_t>(b) * S;
+  const int32_t* stg = a.stack + static_cast<int64_t>(b) * S;
   int live = 0;
+  int nold = 0, p = -1, top = 0;
   if (tid < W) {
-    sh.nold[tid] = a.nblk[r0 + tid];
-    int p = __ldcg(bi + r0 + tid);                        // a fused caller wrote it in this kernel
+    nold = a.nblk[r0 + tid];
+    p = __ldcg(bi + r0 + tid);                            // a fused caller wrote it in this kernel
+  }
+  if (tid == 0) top = a.top[b];
+  for (int i0 = 0; i0 < nt || i0 < S; i0 += NT * LU) {
+    int tv[LU], rv[LU], sv[LU];
+#pragma unroll
+    for (int u = 0; u < LU; ++u) {
+      const int i = i0 + u * NT + tid;
+      tv[u] = i < nt ? tab[i] : 0;
+      rv[u] = i < S ? rcg[i] : 0;
+      sv[u] = i < S ? stg[i] : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < LU; ++u) {
+      const int i = i0 + u * NT + tid;
+      if (i < nt) old[i] = tv[u];
+      if (i < S) {
+        rc[i] = rv[u];
+        rc0[i] = rv[u];
+        stk[i] = sv[u];
+      }
+    }
+  }
+  if (tid < W) {
+    sh.nold[tid] = nold;
     if (p >= 0) {
       live = 1;
       if (p < r0 || p >= r0 + W) {
@@ -59,13 +90,7 @@ __device__ void paged_remap_sentence(const PagedArgs& a, int b, const int32_t* b
     }
     sh.par[tid] = p;
   }
-  for (int i = tid; i < W * MB; i += NT) old[i] = a.table[static_cast<int64_t>(r0) * MB + i];
-  for (int j = tid; j < S; j += NT) {
-    rc[j] = a.refcnt[static_cast<int64_t>(b) * S + j];
-    rc0[j] = rc[j];
-    stk[j] = a.stack[static_cast<int64_t>(b) * S + j];
-  }
-  if (tid == 0) sh.top = a.top[b];
+  if (tid == 0) sh.top = top;
   if (!__syncthreads_or(live)) {                          // a finished sentence: nothing moves
     if (tid < W) a.tasks[r0 + tid] = make_int4(0, 0, 0, 0);
     return;
