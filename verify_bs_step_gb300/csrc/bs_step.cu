@@ -64,6 +64,18 @@ constexpr int MG_NW = MG_NT / 32;
 constexpr float LN2_HI = 0.693147182464599609375f;
 constexpr float LN2_LO = -1.904654299957768e-09f;
 
+// Two fp32 lanes at once (PTX fma.rn.f32x2 / add.rn.f32x2, sm_100 and later): a0, a1 <-
+// a0 * b + c, a1 * b + c; a0, a1 <- a0 + b0, a1 + b1.  Each lane rounds as the scalar op.
+__device__ __forceinline__ void fma2(float& a0, float& a1, float b, float c) {
+  asm("{.reg .b64 x, y, z; mov.b64 x, {%0, %1}; mov.b64 y, {%2, %2}; mov.b64 z, {%3, %3};"
+      " fma.rn.f32x2 x, x, y, z; mov.b64 {%0, %1}, x;}"
+      : "+f"(a0), "+f"(a1) : "f"(b), "f"(c));
+}
+__device__ __forceinline__ void add2(float& a0, float& a1, float b0, float b1) {
+  asm("{.reg .b64 x, y; mov.b64 x, {%0, %1}; mov.b64 y, {%2, %3}; add.rn.f32x2 x, x, y; mov.b64 {%0, %1}, x;}"
+      : "+f"(a0), "+f"(a1) : "f"(b0), "f"(b1));
+}
+
 // Merge (M, l) pairs in the log2 domain: sum = l * 2^M.
 __device__ __forceinline__ void lse_merge(float& M, float& l, float M2, float l2) {
   const float Mn = fmaxf(M, M2);
@@ -156,6 +168,9 @@ struct BsShared {                              // the stream kernel
   u64 cm_key[32];
   float cm_c[32];
   int cm_w[32], cm_sel[32];
+  // cluster mode: the merge's decisions, read by every thread of the first CTA for the gather
+  int cm_nbrow[WMAX], cm_fsrc[WMAX], cm_nbtok[WMAX];
+  int cm_gather;
   // cluster mode: the merge's inputs this kernel does not write, prefetched at its start
   int pf_tile[PF_TILE];
   double pf_fns[WMAX], pf_fworst;
@@ -494,14 +509,23 @@ __device__ void finish_segment(const BsArgs& a, BsShared& sh, int s, int lane) {
 }
 
 // All consumers (after a consumer barrier): publish slots [0, ns).
+// Warp s resolves slot s and, unless its queue must be rescanned, finishes it at once; the
+// rescans (every consumer thread) follow the one barrier, each finished by its slot's warp.
 template <typename T, int VEC, bool BIGK>
 __device__ void publish_slots(const BsArgs& a, BsShared& sh, int ns) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (warp < ns && !sh.seg_skip[warp]) resolve_tiles<T, VEC, BIGK>(a, sh, warp, lane);
+  if (warp < ns) {
+    if (!sh.seg_skip[warp]) resolve_tiles<T, VEC, BIGK>(a, sh, warp, lane);
+    __syncwarp();
+    if (sh.seg_skip[warp] || sh.mode[warp] != 1) finish_segment(a, sh, warp, lane);
+  }
   named_sync(BAR_CONSUMERS, BS_NC);
-  for (int s = 0; s < ns; ++s)
-    if (!sh.seg_skip[s] && sh.mode[s] == 1) rescan_segment<T, VEC>(a, sh, s);
-  if (warp < ns) finish_segment(a, sh, warp, lane);
+  for (int s = 0; s < ns; ++s) {
+    if (!sh.seg_skip[s] && sh.mode[s] == 1) {      // the same for every thread
+      rescan_segment<T, VEC>(a, sh, s);
+      if (warp == s) finish_segment(a, sh, s, lane);
+    }
+  }
 }
 
 // The consumers: every chunk of the range, one row segment after the other.  Nothing in
@@ -658,13 +682,24 @@ __device__ void consume(const BsArgs& a, BsShared& sh, int64_t e0, int64_t e1) {
           float x[VEC];
           if constexpr (TMA) Vec16<T>::unpack(q[u], x);
           else x[0] = xs[u];
+          if constexpr (VEC == 8) {                // bf16: the exponents' arguments and sums in pairs
 #pragma unroll
-          for (int e2 = 0; e2 < VEC; ++e2) x[e2] = ex2(fmaf(x[e2], LOG2E_F, -M));
+            for (int e2 = 0; e2 < VEC; e2 += 2) fma2(x[e2], x[e2 + 1], LOG2E_F, -M);
 #pragma unroll
-          for (int w = 1; w < VEC; w <<= 1)
+            for (int e2 = 0; e2 < VEC; ++e2) x[e2] = ex2(x[e2]);
+            add2(x[0], x[1], x[2], x[3]);
+            add2(x[4], x[5], x[6], x[7]);
+            add2(x[0], x[1], x[4], x[5]);
+            acc[u] = x[0] + x[1];
+          } else {
 #pragma unroll
-            for (int e2 = 0; e2 + w < VEC; e2 += 2 * w) x[e2] += x[e2 + w];
-          acc[u] = x[0];
+            for (int e2 = 0; e2 < VEC; ++e2) x[e2] = ex2(fmaf(x[e2], LOG2E_F, -M));
+#pragma unroll
+            for (int w = 1; w < VEC; w <<= 1)
+#pragma unroll
+              for (int e2 = 0; e2 + w < VEC; e2 += 2 * w) x[e2] += x[e2 + w];
+            acc[u] = x[0];
+          }
         }
 #pragma unroll
         for (int w = 1; w < BS_U; w <<= 1)
@@ -780,12 +815,14 @@ __device__ void cluster_prefetch(const BsArgs& a, BsShared& sh, int b, int lane)
 }
 
 // One warp: sentence b's merge from the cluster's row results (W * K <= 32; lane = w*K + i).
-__device__ void cluster_merge_sentence(const BsArgs& a, BsShared& sh, int b, int lane) {
+// Lane 0 returns the step's finished-sentence count before this sentence (old_cnt) and
+// whether it is done now; the sequence gather is left to cluster_gather.
+__device__ void cluster_merge_sentence(const BsArgs& a, BsShared& sh, int b, int lane, unsigned& old_cnt,
+                                       int& done_now) {
   namespace cg = cooperative_groups;
   cg::cluster_group cl = cg::this_cluster();
   const int W = a.W, K = a.K, RPC = W / a.cluster;
   const int r0 = b * W, t = a.t, ld = a.seq_ld;
-  int* tile = reinterpret_cast<int*>(&sh.ring[0][0]);
   // ---- one round of loads: the rows' results (distributed shared memory), the sentence state
   const int wl = min(lane / K, W - 1), il = lane - wl * K;
   u64 kl = 0ull;
@@ -806,8 +843,8 @@ __device__ void cluster_merge_sentence(const BsArgs& a, BsShared& sh, int b, int
   int fcount = sh.pf_fcount, fnext = sh.pf_fnext;
   float fworst = static_cast<float>(sh.pf_fworst);
   const bool was_done = sh.pf_done != 0;
-  unsigned old_cnt = 0;
-  int done_now = 1;
+  old_cnt = 0;
+  done_now = 1;
   int nb_row = r0, nb_tok = a.pad, f_src = -1;     // lane w < W: new beam w, finished slot w's source
   float nb_score = 0.f;
   if (!was_done) {
@@ -936,36 +973,13 @@ __device__ void cluster_merge_sentence(const BsArgs& a, BsShared& sh, int b, int
       a.fin_worst[b] = static_cast<double>(fworst);
       a.done[b] = done_now;
     }
-    // sequences: the parents' columns [0, t) gathered in place, staged one column tile at a
-    // time, then the new token at column t
-    const int TWp = PF_TILE / W, ncp = min(t, TWp);
-    for (int w = 0; w < W; ++w) {                  // the prefetched columns
-      const int pr = __shfl_sync(FULL, nb_row, w) - r0;
-      const int fs = __shfl_sync(FULL, f_src, w);
-      for (int c = lane; c < ncp; c += 32) {
-        a.seqs[static_cast<int64_t>(r0 + w) * ld + c] = sh.pf_tile[pr * TWp + c];
-        if (fs >= 0) a.fin_tok[static_cast<int64_t>(r0 + w) * ld + c] = sh.pf_tile[(fs - r0) * TWp + c];
-      }
+    // the sequence gather: every thread of the CTA, from these decisions
+    if (lane < W) {
+      sh.cm_nbrow[lane] = nb_row;
+      sh.cm_fsrc[lane] = f_src;
+      sh.cm_nbtok[lane] = nb_tok;
     }
-    const int TWc = CM_TILE / W;
-    for (int c0 = ncp; c0 < t; c0 += TWc) {        // the rest, staged through the free ring
-      const int nc = min(TWc, t - c0);
-      for (int i = lane; i < W * nc; i += 32) {
-        const int w = i / nc, c = i - w * nc;
-        tile[w * TWc + c] = __ldcg(a.seqs + static_cast<int64_t>(r0 + w) * ld + c0 + c);
-      }
-      __syncwarp();
-      for (int w = 0; w < W; ++w) {
-        const int pr = __shfl_sync(FULL, nb_row, w) - r0;
-        const int fs = __shfl_sync(FULL, f_src, w);
-        for (int c = lane; c < nc; c += 32) {
-          a.seqs[static_cast<int64_t>(r0 + w) * ld + c0 + c] = tile[pr * TWc + c];
-          if (fs >= 0) a.fin_tok[static_cast<int64_t>(r0 + w) * ld + c0 + c] = tile[(fs - r0) * TWc + c];
-        }
-      }
-      __syncwarp();
-    }
-    if (lane < W) a.seqs[static_cast<int64_t>(r0 + lane) * ld + t] = nb_tok;
+    if (lane == 0) sh.cm_gather = 1;
   } else {
     if (lane == 0) old_cnt = atomicAdd(reinterpret_cast<unsigned*>(a.done_count), (1u << 16) | 1u);
     if (lane < W) {
@@ -974,14 +988,42 @@ __device__ void cluster_merge_sentence(const BsArgs& a, BsShared& sh, int b, int
       a.scores[r0 + lane] = 0.f;
       a.seqs[static_cast<int64_t>(r0 + lane) * ld + t] = a.pad;
     }
+    if (lane == 0) sh.cm_gather = 0;
   }
-  // the last sentence of the step reports whether all are finished
-  if (lane == 0 && (old_cnt >> 16) == static_cast<unsigned>(a.B - 1)) {
-    const int all = static_cast<int>((old_cnt & 0xffffu) + done_now) == a.B;
-    *a.all_done_dev = all;
-    if (a.all_done_out) *a.all_done_out = all;
-    *a.done_count = 0;
+}
+
+// Every thread of the cluster's first CTA, after the merge's decisions (and its prefetch of
+// the first sequence columns) are visible: the parents' columns [0, t) gathered in place --
+// the prefetched ones directly, the rest staged one column tile at a time through the free
+// ring -- and the new token at column t; the finished hypotheses' tokens likewise.
+__device__ void cluster_gather(const BsArgs& a, BsShared& sh, int b) {
+  if (!sh.cm_gather) return;                       // the same for every thread
+  const int W = a.W, r0 = b * W, t = a.t, ld = a.seq_ld, tid = threadIdx.x;
+  int* tile = reinterpret_cast<int*>(&sh.ring[0][0]);
+  const int TWp = PF_TILE / W, ncp = min(t, TWp);
+  for (int i = tid; i < W * ncp; i += BS_NT) {
+    const int w = i / ncp, c = i - w * ncp;
+    const int pr = sh.cm_nbrow[w] - r0, fs = sh.cm_fsrc[w];
+    a.seqs[static_cast<int64_t>(r0 + w) * ld + c] = sh.pf_tile[pr * TWp + c];
+    if (fs >= 0) a.fin_tok[static_cast<int64_t>(r0 + w) * ld + c] = sh.pf_tile[(fs - r0) * TWp + c];
   }
+  const int TWc = CM_TILE / W;
+  for (int c0 = ncp; c0 < t; c0 += TWc) {
+    const int nc = min(TWc, t - c0);
+    __syncthreads();                               // the tile's previous contents are written out
+    for (int i = tid; i < W * nc; i += BS_NT) {
+      const int w = i / nc, c = i - w * nc;
+      tile[w * TWc + c] = __ldcg(a.seqs + static_cast<int64_t>(r0 + w) * ld + c0 + c);
+    }
+    __syncthreads();
+    for (int i = tid; i < W * nc; i += BS_NT) {
+      const int w = i / nc, c = i - w * nc;
+      const int pr = sh.cm_nbrow[w] - r0, fs = sh.cm_fsrc[w];
+      a.seqs[static_cast<int64_t>(r0 + w) * ld + c0 + c] = tile[pr * TWc + c];
+      if (fs >= 0) a.fin_tok[static_cast<int64_t>(r0 + w) * ld + c0 + c] = tile[(fs - r0) * TWc + c];
+    }
+  }
+  if (tid < W) a.seqs[static_cast<int64_t>(r0 + tid) * ld + t] = sh.cm_nbtok[tid];
 }
 
 template <typename T, bool TMA, bool FUSE>
@@ -1034,7 +1076,20 @@ __global__ void __launch_bounds__(BS_NT, 1) bs_cluster_kernel(const BsArgs a) {
   }
   __syncwarp();
   cooperative_groups::this_cluster().sync();       // every CTA's row results are in its shared memory
-  if (c == 0 && threadIdx.x < 32) cluster_merge_sentence(a, sh, b, threadIdx.x);
+  if (c == 0) {
+    unsigned old_cnt = 0;
+    int done_now = 0;
+    if (threadIdx.x < 32) cluster_merge_sentence(a, sh, b, threadIdx.x, old_cnt, done_now);
+    __syncthreads();                               // the decisions, for the gather by every thread
+    cluster_gather(a, sh, b);
+    // the last sentence of the step reports whether all are finished
+    if (threadIdx.x == 0 && (old_cnt >> 16) == static_cast<unsigned>(a.B - 1)) {
+      const int all = static_cast<int>((old_cnt & 0xffffu) + done_now) == a.B;
+      *a.all_done_dev = all;
+      if (a.all_done_out) *a.all_done_out = all;
+      *a.done_count = 0;
+    }
+  }
   cooperative_groups::this_cluster().sync();       // keep them readable until the merge is done
   if (FUSE && c == 0) {
     // the paged KV remap of the sentence, on the step's beam_idx just written; the ring is
