@@ -56,7 +56,8 @@ enum {
   VBS_EALIGN = -5,   /* a pointer or stride is not aligned as the call needs */
   VBS_ETIMEOUT = -6, /* a bounded device-side wait gave up */
   VBS_EINPUT = -7,   /* the input data broke a precondition (NaN / +inf logits, ...) */
-  VBS_ESCRATCH = -8  /* the problem is larger than bs_expand_static's static scratch allows */
+  VBS_ESCRATCH = -8, /* the problem is larger than bs_expand_static's static scratch allows */
+  VBS_EBOUNDS = -9   /* a device bounds check failed (only the checked build, libvbs_checked.so, checks) */
 };
 
 enum { VBS_F32 = 0, VBS_BF16 = 1 };
@@ -477,6 +478,20 @@ int vbs_peak_copy(const void* src, void* dst, int64_t bytes, int grid, vbs_strea
  *   VBS_EALIGN (src not 16-byte aligned, bytes not a multiple of 16), VBS_ECUDA.
  */
 int vbs_peak_read(const void* src, int64_t bytes, int grid, int mode, uint32_t* sink, vbs_stream_t stream);
+
+/*
+ * The device bounds checks of the checked build.  The library can be built a second
+ * time with VBS_CHECKED defined (libvbs_checked.so): then the indexed accesses whose index
+ * comes from data (the streamed row ranges, partial slots, merge outputs and sequence
+ * gathers, the KV parents and pool blocks, the verify queue's slots) are guarded; a
+ * failed guard skips the access, sets VBS_EBOUNDS in the call's status word and records
+ * the first failure.  Synchronises the device, then sets *checked (1 in the checked build,
+ * 0 otherwise), and *site / *index of the first failed check since the last call (-1 / -1
+ * when none; the record is then cleared).  The pages have no counterpart: this is a test
+ * aid, the checks stand in for a memory checker.
+ * Errors: VBS_EINVAL (NULL), VBS_ECUDA.
+ */
+int vbs_checked_record(int* checked, int* site, int64_t* index);
 
 #ifdef __cplusplus
 }

@@ -21,9 +21,10 @@ F32, BF16 = 0, 1
 LP_GNMT, LP_POWER = 0, 1
 BPD_EXACT, BPD_TOPK, BPD_DISTANCE = 0, 1, 2
 ES_FALSE, ES_TRUE, ES_NEVER = 0, 1, 2
-OK, EINVAL, ECUDA, ENOMEM, ESTATE, EALIGN, ETIMEOUT, EINPUT, ESCRATCH = 0, -1, -2, -3, -4, -5, -6, -7, -8
+OK, EINVAL, ECUDA, ENOMEM, ESTATE, EALIGN, ETIMEOUT, EINPUT, ESCRATCH, EBOUNDS = 0, -1, -2, -3, -4, -5, -6, -7, -8, -9
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libvbs.so")
+CHECKED_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libvbs_checked.so")
 
 _c_int, _c_i64, _c_f, _vp = ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
 _pp = ctypes.POINTER(ctypes.c_void_p)
@@ -70,6 +71,7 @@ SIGNATURES = {
                                    _vp]),
     "vbs_peak_copy": (_c_int, [_vp, _vp, _c_i64, _c_int, _vp]),
     "vbs_peak_read": (_c_int, [_vp, _c_i64, _c_int, _c_int, _vp, _vp]),
+    "vbs_checked_record": (_c_int, [ctypes.POINTER(_c_int), ctypes.POINTER(_c_int), ctypes.POINTER(_c_i64)]),
 }
 
 _LIB = None
@@ -94,6 +96,32 @@ def lib():
             fn.restype, fn.argtypes = res, args
         _LIB = L
     return _LIB
+
+
+def load_checked():
+    """The checked build (libvbs_checked.so: device bounds checks on), loaded with the same
+    signatures; swap it in with `use_library(...)`."""
+    if not os.path.exists(CHECKED_LIB_PATH):
+        raise RuntimeError(f"{CHECKED_LIB_PATH} is missing: build it with `python -m verify_bs_step_gb300._build`")
+    L = ctypes.CDLL(CHECKED_LIB_PATH)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(L, name)
+        fn.restype, fn.argtypes = res, args
+    return L
+
+
+def use_library(L):
+    """Make every call of this module go to library L (returns the one it replaces)."""
+    global _LIB
+    old, _LIB = _LIB, L
+    return old
+
+
+def checked_record():
+    """(checked build?, site, index) of the first failed device bounds check since the last call."""
+    c, site, idx = _c_int(), _c_int(), _c_i64()
+    _check(lib().vbs_checked_record(ctypes.byref(c), ctypes.byref(site), ctypes.byref(idx)), "vbs_checked_record")
+    return bool(c.value), site.value, idx.value
 
 
 def _check(st: int, what: str):

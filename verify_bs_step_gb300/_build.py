@@ -18,6 +18,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build", "vbs")
 LIB = os.path.join(HERE, "libvbs.so")
+BUILD_CHECKED = os.path.join(ROOT, "_build", "vbs_checked")
+LIB_CHECKED = os.path.join(HERE, "libvbs_checked.so")
 
 SOURCES = ["api.cu", "bs_step.cu", "kv.cu", "bpd.cu", "peak.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -39,17 +41,21 @@ def _stale(obj: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(verbose: bool = False, ptxas_info: bool = False, force: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, ptxas_info: bool = False, force: bool = False, checked: bool = False) -> str:
+    """Build libvbs.so (or, with checked, libvbs_checked.so: VBS_CHECKED defined, device bounds
+    checks on) and return its path."""
+    build_dir, lib_path = (BUILD_CHECKED, LIB_CHECKED) if checked else (BUILD, LIB)
+    extra = ["-DVBS_CHECKED"] if checked else []
+    os.makedirs(build_dir, exist_ok=True)
     headers = [os.path.join(CSRC, h) for h in os.listdir(CSRC) if h.endswith((".h", ".cuh"))]
     headers.append(os.path.join(INCLUDE, "vbs.h"))
     cc = nvcc()
     jobs = []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src.replace(".cu", ".o"))
+        o = os.path.join(build_dir, src.replace(".cu", ".o"))
         if force or ptxas_info or _stale(o, [s] + headers):
-            cmd = [cc, *ARCH, *FLAGS, "-c", s, "-o", o]
+            cmd = [cc, *ARCH, *FLAGS, *extra, "-c", s, "-o", o]
             if ptxas_info:
                 cmd.insert(1, "-Xptxas=-v")
             jobs.append((src, cmd))
@@ -61,15 +67,16 @@ def build(verbose: bool = False, ptxas_info: bool = False, force: bool = False) 
                 sys.stderr.write(r.stdout + r.stderr)
             if r.returncode:
                 raise RuntimeError(f"nvcc failed on {futs[f]}")
-    objs = [os.path.join(BUILD, s.replace(".cu", ".o")) for s in SOURCES]
-    if force or jobs or _stale(LIB, objs):
-        cmd = [cc, *ARCH, "-shared", "-o", LIB, *objs]
+    objs = [os.path.join(build_dir, s.replace(".cu", ".o")) for s in SOURCES]
+    if force or jobs or _stale(lib_path, objs):
+        cmd = [cc, *ARCH, "-shared", "-o", lib_path, *objs]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode:
             sys.stderr.write(r.stdout + r.stderr)
             raise RuntimeError("link failed")
-    return LIB
+    return lib_path
 
 
 if __name__ == "__main__":
     print(build(verbose="-v" in sys.argv, ptxas_info="--ptxas" in sys.argv, force="--force" in sys.argv))
+    print(build(force="--force" in sys.argv, checked=True))

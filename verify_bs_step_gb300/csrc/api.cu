@@ -84,6 +84,7 @@ VBS_EXPORT const char* vbs_strerror(int status) {
     case VBS_ETIMEOUT: return "a bounded device-side wait gave up";
     case VBS_EINPUT: return "input data broke a precondition";
     case VBS_ESCRATCH: return "problem too large for the static scratch of bs_expand_static";
+    case VBS_EBOUNDS: return "a device bounds check failed (checked build)";
     default: return "unknown status";
   }
 }
@@ -740,4 +741,29 @@ VBS_EXPORT int vbs_peak_read(const void* src, int64_t bytes, int grid, int mode,
   int* status = nullptr;
   if (cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_stateless_status) != cudaSuccess) return VBS_ECUDA;
   return vbs::launch_peak_read(src, bytes, grid, mode, sink, status, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// =====================================================================================
+// the checked build's bounds-check record
+// =====================================================================================
+
+VBS_EXPORT int vbs_checked_record(int* checked, int* site, int64_t* index) {
+  if (!checked || !site || !index) return VBS_EINVAL;
+#ifdef VBS_CHECKED
+  *checked = 1;
+#else
+  *checked = 0;
+#endif
+  *site = -1;
+  *index = -1;
+  if (cudaDeviceSynchronize() != cudaSuccess) return VBS_ECUDA;
+  const unsigned long long recs[3] = {vbs::bs_check_record(), vbs::kv_check_record(), vbs::bpd_check_record()};
+  for (unsigned long long r : recs) {
+    if (r == ~0ull) return VBS_ECUDA;
+    if (r && *site < 0) {
+      *site = static_cast<int>(r >> 40) - 1;
+      *index = static_cast<int64_t>(r & 0xffffffffffull);
+    }
+  }
+  return VBS_OK;
 }

@@ -397,6 +397,7 @@ __global__ void __launch_bounds__(BPD_RT, 3) bpd_verify_queue_kernel(const void*
     __syncthreads();
     if (b >= B) break;
     if (tid == 0) next_b = static_cast<int>(gridDim.x) + atomicAdd(&g_bpd_next_chain, 1);
+    if (!VBS_CHECK(b >= 0, 21, b, status)) break;
     const char* base = reinterpret_cast<const char*>(logits) + static_cast<int64_t>(b) * k * k * row_bytes;
     const int32_t* props = proposals + static_cast<int64_t>(b) * k;
     int checks = k - 1;                            // proposals up to an EOS need no checks past it
@@ -433,7 +434,8 @@ __global__ void __launch_bounds__(BPD_RT, 3) bpd_verify_queue_kernel(const void*
         if (!tag) tag = static_cast<u64>(*reinterpret_cast<volatile unsigned*>(&g_bpd_epoch) + 1u) << 32;
         const int slot = atomicAdd(&g_bpd_ready_tail, k - 1);
         for (int h = 1; h < k; ++h)
-          st_release_u64(&g_bpd_ready[slot + h - 1], tag | (static_cast<u64>(b) << 5) | static_cast<u64>(h));
+          if (VBS_CHECK(slot + h - 1 < BPD_MAX_READY, 20, slot + h - 1, status))
+            st_release_u64(&g_bpd_ready[slot + h - 1], tag | (static_cast<u64>(b) << 5) | static_cast<u64>(h));
       }
     }
   }
@@ -443,7 +445,7 @@ __global__ void __launch_bounds__(BPD_RT, 3) bpd_verify_queue_kernel(const void*
     if (tid == 0) {
       const int r = atomicAdd(&g_bpd_ready_head, 1);
       s_unit = r;
-      if (r < n_rows) {
+      if (r < n_rows && VBS_CHECK(r < BPD_MAX_READY, 22, r, status)) {
         u64 e = 0;
         u32 it = 0;
         while (((e = ld_acquire_u64(&g_bpd_ready[r])) >> 32) != (tag >> 32)) {
@@ -545,5 +547,7 @@ int launch_bpd_verify(const void* logits, const int32_t* proposals, int B, int k
   return vec_ok ? launch_verify<float, true>(logits, proposals, B, k, V, eos, crit, khat, next, status, num_sms, s)
                 : launch_verify<float, false>(logits, proposals, B, k, V, eos, crit, khat, next, status, num_sms, s);
 }
+
+unsigned long long bpd_check_record() { return read_check_record(); }
 
 }  // namespace vbs

@@ -131,4 +131,9 @@ int launch_bpd_verify(const void* logits, const int32_t* proposals, int B, int k
 int launch_peak_copy(const void* src, void* dst, int64_t bytes, int grid, cudaStream_t s);
 int launch_peak_read(const void* src, int64_t bytes, int grid, int mode, uint32_t* sink, int* status, cudaStream_t s);
 
+// the first failed device bounds check of each file in the checked build (0: none)
+unsigned long long bs_check_record();
+unsigned long long kv_check_record();
+unsigned long long bpd_check_record();
+
 }  // namespace vbs

@@ -343,7 +343,8 @@ __device__ void produce(const BsArgs& a, BsShared& sh, int64_t e0, int64_t e1) {
     const int slot = c % NSTAGE;
     if (c >= NSTAGE && !mbar_wait(&sh.empty[slot], static_cast<u32>(((c / NSTAGE) + 1) & 1)))
       set_status(a.status, VBS_ETIMEOUT);
-    const u32 bytes = skip ? 0u : static_cast<u32>(ch.len * Elem<T>::BYTES);
+    u32 bytes = skip ? 0u : static_cast<u32>(ch.len * Elem<T>::BYTES);
+    if (bytes && !VBS_CHECK(ch.r < a.R && ch.v0 >= 0 && ch.v0 + ch.len <= a.V, 1, ch.r, a.status)) bytes = 0;
     sh.stage_skip[slot] = skip ? 1 : 0;               // published by the arrive below
     mbar_expect_tx(&sh.full[slot], bytes);
     if (bytes) {
@@ -478,7 +479,8 @@ __device__ void finish_segment(const BsArgs& a, BsShared& sh, int s, int lane) {
     const int r = sh.seg_r[s];
     const int64_t pslot =
         a.cluster ? 0 : static_cast<int64_t>(r) * a.P + (static_cast<int>(blockIdx.x) - a.row_p0[r]);
-    u64* out = a.cluster ? sh.rk[s] : a.part_key + pslot * K;   // cluster mode: whole rows stay in shared memory
+    const bool pslot_ok = VBS_CHECK(pslot >= 0 && pslot < static_cast<int64_t>(a.R) * a.P, 2, pslot, a.status);
+    u64* out = a.cluster ? sh.rk[s] : (pslot_ok ? a.part_key + pslot * K : sh.fin[s]);   // cluster mode: in shared memory
     if (mode == 0) {
       const int cnt = sh.fcnt[s];
       for (int j = lane; j < cnt; j += 32) {
@@ -496,7 +498,7 @@ __device__ void finish_segment(const BsArgs& a, BsShared& sh, int s, int lane) {
       if (a.cluster) {
         sh.rM[s] = Mw;
         sh.rl[s] = lw;
-      } else {
+      } else if (pslot_ok) {
         a.part_M[pslot] = Mw;
         a.part_l[pslot] = lw;
       }
@@ -959,7 +961,7 @@ __device__ void cluster_merge_sentence(const BsArgs& a, BsShared& sh, int b, int
     done_now = done ? 1 : 0;
     // the step's finished-sentence count, issued before the writes
     if (lane == 0) old_cnt = atomicAdd(reinterpret_cast<unsigned*>(a.done_count), (1u << 16) | done_now);
-    if (lane < W) {
+    if (lane < W && VBS_CHECK(r0 + lane < a.R && nb_row >= r0 && nb_row < r0 + W, 3, nb_row, a.status)) {
       a.beam_idx[r0 + lane] = nb_row;
       a.tokens[r0 + lane] = nb_tok;
       a.scores[r0 + lane] = nb_score;
@@ -1004,6 +1006,7 @@ __device__ void cluster_gather(const BsArgs& a, BsShared& sh, int b) {
   for (int i = tid; i < W * ncp; i += BS_NT) {
     const int w = i / ncp, c = i - w * ncp;
     const int pr = sh.cm_nbrow[w] - r0, fs = sh.cm_fsrc[w];
+    if (!VBS_CHECK(pr >= 0 && pr < W && (fs < 0 || (fs >= r0 && fs < r0 + W)) && c < ld, 4, pr, a.status)) continue;
     a.seqs[static_cast<int64_t>(r0 + w) * ld + c] = sh.pf_tile[pr * TWp + c];
     if (fs >= 0) a.fin_tok[static_cast<int64_t>(r0 + w) * ld + c] = sh.pf_tile[(fs - r0) * TWp + c];
   }
@@ -1019,6 +1022,7 @@ __device__ void cluster_gather(const BsArgs& a, BsShared& sh, int b) {
     for (int i = tid; i < W * nc; i += BS_NT) {
       const int w = i / nc, c = i - w * nc;
       const int pr = sh.cm_nbrow[w] - r0, fs = sh.cm_fsrc[w];
+      if (!VBS_CHECK(pr >= 0 && pr < W && (fs < 0 || (fs >= r0 && fs < r0 + W)), 4, pr, a.status)) continue;
       a.seqs[static_cast<int64_t>(r0 + w) * ld + c0 + c] = tile[pr * TWc + c];
       if (fs >= 0) a.fin_tok[static_cast<int64_t>(r0 + w) * ld + c0 + c] = tile[(fs - r0) * TWc + c];
     }
@@ -1389,6 +1393,9 @@ __device__ void merge_sentence(const BsArgs& a, MergeShared& sm, int b, int done
       }
       for (int i = tid; i < W * nc; i += NT) {
         const int w = i / nc, c = i - w * nc;
+        if (!VBS_CHECK(sm.nb_row[w] >= r0 && sm.nb_row[w] < r0 + W &&
+                           (sm.f_src[w] < 0 || (sm.f_src[w] >= r0 && sm.f_src[w] < r0 + W)), 5, sm.nb_row[w], a.status))
+          continue;
         a.seqs[static_cast<int64_t>(r0 + w) * ld + c0 + c] = sm.tile[(sm.nb_row[w] - r0) * TW + c];
         if (sm.f_src[w] >= 0)
           a.fin_tok[static_cast<int64_t>(r0 + w) * ld + c0 + c] = sm.tile[(sm.f_src[w] - r0) * TW + c];
@@ -1513,6 +1520,7 @@ __global__ void bs_finalize_kernel(const BsArgs a, const float* scores, const in
   for (int j = 0; j < n_ret; ++j) {
     const int q = s_order[j];
     const int n = f_ntok[q];
+    if (!VBS_CHECK(f_src[q] < a.R && q < W, 6, f_src[q], a.status)) continue;
     const int32_t* src = f_src[q] >= 0 ? seqs + static_cast<int64_t>(f_src[q]) * ld
                                        : a.fin_tok + static_cast<int64_t>(r0 + q) * ld;
     int32_t* dst = out_seqs + (static_cast<int64_t>(b) * n_ret + j) * ld;
@@ -1870,6 +1878,7 @@ int launch_bs_finalize(const BsArgs& a, const float* scores, const int32_t* seqs
 }
 
 int bs_threads_per_cta() { return BS_NT; }
+unsigned long long bs_check_record() { return read_check_record(); }
 int bs_ctas_per_sm() { return 1; }
 
 // ---------------------------------------------------------------------------------------

@@ -268,6 +268,43 @@ __device__ __forceinline__ void set_status(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
 
+// ------------------------------------------------------------------------------------
+// device bounds checks of the checked build (compiled with VBS_CHECKED)
+// ------------------------------------------------------------------------------------
+//
+// VBS_CHECK(cond, site, index, status) guards one indexed access: in the checked build a
+// false condition records (site, index) in this translation unit's record (the first
+// failure wins), sets VBS_EBOUNDS in the status word and yields false, so the caller skips
+// the access; the normal build compiles it to true.  Sites are numbered per file; the
+// record is read by vbs_checked_record().
+
+#ifdef VBS_CHECKED
+static __device__ unsigned long long g_check_record;   // ((site + 1) << 40) | index, 0 = none
+
+__device__ __forceinline__ bool check_impl(bool ok, int site, long long index, int* status) {
+  if (!ok) {
+    const unsigned long long rec = (static_cast<unsigned long long>(site + 1) << 40) |
+                                   (static_cast<unsigned long long>(index) & 0xffffffffffull);
+    atomicCAS(&g_check_record, 0ull, rec);
+    set_status(status, VBS_EBOUNDS);
+  }
+  return ok;
+}
+#define VBS_CHECK(cond, site, index, status) \
+  ::vbs::check_impl(static_cast<bool>(cond), (site), static_cast<long long>(index), (status))
+
+// Read (then clear) this translation unit's record: 0 if no check failed.
+static inline unsigned long long read_check_record() {
+  unsigned long long rec = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&rec, g_check_record, sizeof(rec)) != cudaSuccess) return ~0ull;
+  cudaMemcpyToSymbol(g_check_record, &zero, sizeof(zero));
+  return rec;
+}
+#else
+#define VBS_CHECK(cond, site, index, status) true
+static inline unsigned long long read_check_record() { return 0; }
+#endif
+
 // Raise a kernel's dynamic shared-memory limit once per device (the attribute is per
 // device and function); `done` holds one bit per device already set.
 template <typename F>

@@ -89,6 +89,7 @@ struct NaiveMap {
   const int32_t* bi;
   int H, rows;
   int64_t seg_stride, copy_bytes, nch;
+  int* status;
   __device__ void operator()(int64_t item, const char*& s, char*& d, u32& bytes) const {
     const int64_t c = item % nch;
     const int64_t seg = item / nch;
@@ -98,6 +99,10 @@ struct NaiveMap {
     const int p = __ldg(bi + r);
     bytes = 0;
     if (p < 0) return;
+    if (p >= rows) {                                  // not a row of the cache: nothing is copied
+      set_status(status, VBS_EINPUT);
+      return;
+    }
     const int64_t off = c * KV_CHUNK;
     const int64_t rem = copy_bytes - off;
     bytes = static_cast<u32>(rem < KV_CHUNK ? rem : KV_CHUNK);
@@ -113,7 +118,7 @@ __global__ void __launch_bounds__(32) kv_naive_bulk_kernel(NaiveMap map, int64_t
 // Element-wise fallback for layouts the bulk engine cannot take (alignment).
 template <typename W>
 __global__ void kv_naive_plain_kernel(const char* src, char* dst, const int32_t* bi, int H, int rows,
-                                      int64_t seg_stride, int64_t copy_words, int64_t n_segs) {
+                                      int64_t seg_stride, int64_t copy_words, int64_t n_segs, int* status) {
   const int64_t total = n_segs * copy_words;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -123,6 +128,10 @@ __global__ void kv_naive_plain_kernel(const char* src, char* dst, const int32_t*
     const int64_t lkv = seg / (static_cast<int64_t>(H) * rows);
     const int p = __ldg(bi + r);
     if (p < 0) continue;
+    if (p >= rows) {                                  // not a row of the cache: nothing is copied
+      set_status(status, VBS_EINPUT);
+      continue;
+    }
     const W* s = reinterpret_cast<const W*>(src + ((lkv * rows + p) * H + h) * seg_stride);
     W* d = reinterpret_cast<W*>(dst + ((lkv * rows + r) * H + h) * seg_stride);
     d[w] = s[w];
@@ -135,7 +144,7 @@ int launch_kv_naive(const KvGeom& g, const void* src, void* dst, const int32_t* 
   if (g.copy_bytes == 0 || n_segs == 0) return VBS_OK;
   if (bulk_ok) {
     NaiveMap m{static_cast<const char*>(src), static_cast<char*>(dst), beam_idx, g.H, g.rows,
-               g.seg_stride, g.copy_bytes, (g.copy_bytes + KV_CHUNK - 1) / KV_CHUNK};
+               g.seg_stride, g.copy_bytes, (g.copy_bytes + KV_CHUNK - 1) / KV_CHUNK, status};
     const int64_t n_items = n_segs * m.nch;
     const size_t smem = static_cast<size_t>(KV_STAGES) * KV_CHUNK;
     static std::atomic<unsigned long long> attr_done{0};
@@ -148,13 +157,13 @@ int launch_kv_naive(const KvGeom& g, const void* src, void* dst, const int32_t* 
     char* dp = static_cast<char*>(dst);
     if (g.copy_bytes % 4 == 0 && g.seg_stride % 4 == 0 && elem_bytes % 4 == 0)
       kv_naive_plain_kernel<uint32_t><<<static_cast<int>(grid), 256, 0, s>>>(
-          sp, dp, beam_idx, g.H, g.rows, g.seg_stride, g.copy_bytes / 4, n_segs);
+          sp, dp, beam_idx, g.H, g.rows, g.seg_stride, g.copy_bytes / 4, n_segs, status);
     else if (g.copy_bytes % 2 == 0 && g.seg_stride % 2 == 0)
       kv_naive_plain_kernel<uint16_t><<<static_cast<int>(grid), 256, 0, s>>>(
-          sp, dp, beam_idx, g.H, g.rows, g.seg_stride, g.copy_bytes / 2, n_segs);
+          sp, dp, beam_idx, g.H, g.rows, g.seg_stride, g.copy_bytes / 2, n_segs, status);
     else
       kv_naive_plain_kernel<uint8_t><<<static_cast<int>(grid), 256, 0, s>>>(
-          sp, dp, beam_idx, g.H, g.rows, g.seg_stride, g.copy_bytes, n_segs);
+          sp, dp, beam_idx, g.H, g.rows, g.seg_stride, g.copy_bytes, n_segs, status);
   }
   return cudaGetLastError() == cudaSuccess ? VBS_OK : VBS_ECUDA;
 }
@@ -211,11 +220,14 @@ struct CowMap {
   int task_cap;
   int n_runs;                       // L * 2 * H
   int64_t block_bytes, run_bytes, slot_bytes;
+  int64_t n_blocks;                 // blocks in the pool
+  int* status;
   __device__ void operator()(int64_t item, const char*& s, char*& d, u32& bytes) const {
     const int q = static_cast<int>(item / n_runs);
     const int run = static_cast<int>(item % n_runs);
     const int4 t = tasks[q];
     bytes = static_cast<u32>(t.z * slot_bytes);
+    if (bytes && !VBS_CHECK(t.x >= 0 && t.x < n_blocks && t.y >= 0 && t.y < n_blocks, 11, t.x, status)) bytes = 0;
     s = pool + t.x * block_bytes + run * run_bytes;
     d = const_cast<char*>(pool) + t.y * block_bytes + run * run_bytes;
   }
@@ -280,9 +292,12 @@ __global__ void kv_cow_plain_kernel(CowMap map) {
 int launch_kv_paged_cow(const PagedArgs& a, bool bulk_ok, int num_sms, cudaStream_t s) {
   const int n_runs = a.L * 2 * a.H;
   const int64_t run_bytes = static_cast<int64_t>(a.block) * a.slot_bytes;
-  CowMap m{a.pool, a.tasks, a.task_cap, n_runs, a.block_bytes, run_bytes, a.slot_bytes};
+  CowMap m{a.pool, a.tasks, a.task_cap, n_runs, a.block_bytes, run_bytes, a.slot_bytes,
+           static_cast<int64_t>(a.B) * a.S, a.status};
   if (bulk_ok) return launch_pdl(kv_cow_vec_kernel, dim3(num_sms * COW_CTAS_PER_SM), dim3(COW_NT), 0, s, m);
   return launch_pdl(kv_cow_plain_kernel, dim3(num_sms * KV_CTAS_PER_SM), dim3(256), 0, s, m);
 }
+
+unsigned long long kv_check_record() { return read_check_record(); }
 
 }  // namespace vbs
