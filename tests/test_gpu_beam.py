@@ -350,3 +350,27 @@ def test_vocab_shards_limits():
         bs.merge_shards(part.unsqueeze(0).repeat(33, 1))    # more shards than the merge holds (W 4: 32)
     assert e.value.status == vbs.EINVAL
     bs.close()
+
+
+# ------------------------------------------------------------------------------------
+# logits that are not finite: reported in the status word, the context stays usable
+# ------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("B,W,V,dtype", [
+    (3, 2, 64, torch.float32),            # cluster kernel, element path
+    (2, 4, 4096, torch.bfloat16),         # cluster kernel, bulk-copy path
+    (4, 16, 512, torch.bfloat16),         # stream and merge kernels
+])
+@pytest.mark.parametrize("bad", [float("nan"), float("inf")])
+def test_non_finite_logits_are_reported(B, W, V, dtype, bad):
+    import verify_bs_step_gb300 as vbs
+    bs = vbs.BeamSearch(B, W, V, eos=-1, max_len=4, dtype=dtype)
+    g = torch.Generator().manual_seed(B * W + V)
+    x = torch.randn(B * W, V, generator=g)
+    x[0, 7] = bad                          # beam 0 of sentence 0: a row the first step reads
+    bs.step(x.to(dtype).cuda())
+    assert bs.status() == vbs.EINPUT
+    bs.reset()
+    bs.step(torch.randn(B * W, V, generator=g).to(dtype).cuda())
+    assert bs.status() == 0
+    bs.close()
