@@ -581,6 +581,20 @@ def _timed(torch, stream, fn, reps, ahead=True):
     return [a.elapsed_time(b) for a, b in evs]
 
 
+def _looped(torch, stream, fn, reps):
+    """Mean time of `reps` back-to-back calls between two events, queued behind a GPU spin
+    (calls in a row, as in a decode loop: a call's launch may overlap the previous call)."""
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    torch.cuda._sleep(int(2e5) * reps)
+    e0.record(stream)
+    for _ in range(reps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
 def run_extras(args, torch, vbs, synth, dev, stream, peak):
     """Secondary lines: bs_step alone (Llama, T-base), naive KV gather, blockwise verify."""
     import ctypes
@@ -675,10 +689,15 @@ def run_extras(args, torch, vbs, synth, dev, stream, peak):
         byts = [int(((b[2] + k - 1) * V * 2).sum().item()) + B * k * 12 for b in bufs]
         alg = statistics.fmean(byts[(8 + i) % 4] for i in range(reps))
         avg = statistics.fmean(ts)
-        extra["bpd_verify"] = {"B": B, "k": k, "V": V, "avg_us": round(avg * 1e3, 3),
-                               "iters_per_s": round(1e3 / avg, 1), "mean_khat": round(float(bufs[0][2].float().mean()), 3),
-                               "algorithmic_bytes": int(alg), "achieved_gbs": round(alg / (avg / 1e3) / 1e9, 1),
-                               "frac_of_peak": round(alg / (avg / 1e3) / 1e9 / peak, 4)}
+        loop = _looped(torch, stream, verify, reps)
+        extra["bpd_verify"] = {"B": B, "k": k, "V": V, "avg_us": round(loop * 1e3, 3),
+                               "iters_per_s": round(1e3 / loop, 1), "mean_khat": round(float(bufs[0][2].float().mean()), 3),
+                               "algorithmic_bytes": int(alg), "achieved_gbs": round(alg / (loop / 1e3) / 1e9, 1),
+                               "frac_of_peak": round(alg / (loop / 1e3) / 1e9 / peak, 4),
+                               "per_call_us": round(avg * 1e3, 3),
+                               "per_call_frac_of_peak": round(alg / (avg / 1e3) / 1e9 / peak, 4),
+                               "timing": f"avg_us: {reps} calls back to back between two events (a call's launch "
+                                         f"overlaps the previous call); per_call_us: each call between its own events"}
         # the relaxed verify tests of §5 on the same inputs: the rows read are still
         # khat + k - 1 per element, khat now from the relaxed test (taken from the call)
         for name, crit, param in (("bpd_verify_topk2", vbs.BPD_TOPK, 2), ("bpd_verify_distance1", vbs.BPD_DISTANCE, 1)):
@@ -700,10 +719,12 @@ def run_extras(args, torch, vbs, synth, dev, stream, peak):
             byts_r = [int(((kh_r[j] + k - 1) * V * 2).sum().item()) + B * k * 12 for j in range(4)]
             alg_r = statistics.fmean(byts_r[(8 + i) % 4] for i in range(reps))
             avg_r = statistics.fmean(ts)
-            extra[name] = {"criterion": name.split("_")[-1], "avg_us": round(avg_r * 1e3, 3),
+            loop_r = _looped(torch, stream, verify_r, reps)
+            extra[name] = {"criterion": name.split("_")[-1], "avg_us": round(loop_r * 1e3, 3),
                            "mean_khat": round(float(torch.cat(kh_r).float().mean()), 3),
-                           "algorithmic_bytes": int(alg_r), "achieved_gbs": round(alg_r / (avg_r / 1e3) / 1e9, 1),
-                           "frac_of_peak": round(alg_r / (avg_r / 1e3) / 1e9 / peak, 4)}
+                           "algorithmic_bytes": int(alg_r), "achieved_gbs": round(alg_r / (loop_r / 1e3) / 1e9, 1),
+                           "frac_of_peak": round(alg_r / (loop_r / 1e3) / 1e9 / peak, 4),
+                           "per_call_us": round(avg_r * 1e3, 3)}
     return extra
 
 

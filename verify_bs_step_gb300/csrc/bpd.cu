@@ -383,6 +383,11 @@ __global__ void __launch_bounds__(BPD_RT, 3) bpd_verify_queue_kernel(const void*
     best2[1] = 0ull;
   }
   __syncthreads();
+  // launched as a programmatic dependent: the set-up above overlaps the previous kernel in
+  // the stream; every global access (the queue's counters included) comes after it has
+  // completed
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   RowStage st{bpd_smem, bar, 0u, best2, 0u};
   u64 tag = 0;                                     // this call's ready-list tag, read when first needed
   const int64_t row_bytes = static_cast<int64_t>(V) * Elem<T>::BYTES;
@@ -467,7 +472,8 @@ __global__ void __launch_bounds__(BPD_RT, 3) bpd_verify_queue_kernel(const void*
     if (tid == 0) next_out[static_cast<int64_t>(b) * k + h] = am;
   }
   // the last CTA out resets the queue and moves the ready list to the next epoch (the next
-  // call on the stream starts once this grid has completed)
+  // call on the stream touches them only after its griddepcontrol.wait, i.e. once this grid
+  // has completed)
   if (tid == 0) {
     if (atomicAdd(&g_bpd_exited, 1) == static_cast<int>(gridDim.x) - 1) {
       g_bpd_next_chain = 0;
@@ -518,9 +524,18 @@ static int launch_queue(int grid, const void* logits, const int32_t* proposals, 
   const int smem = VECTOR ? BPD_BUF : 0;
   static std::atomic<unsigned long long> attr_done{0};   // one per kernel instantiation
   if (VECTOR && !smem_attr_once(bpd_verify_queue_kernel<T, VECTOR, RANK>, BPD_BUF, attr_done)) return VBS_ECUDA;
-  bpd_verify_queue_kernel<T, VECTOR, RANK><<<grid, BPD_RT, smem, s>>>(logits, proposals, B, k, V, eos, crit, khat,
-                                                                     next, status);
-  return cudaGetLastError() == cudaSuccess ? VBS_OK : VBS_ECUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(BPD_RT);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, bpd_verify_queue_kernel<T, VECTOR, RANK>, logits, proposals, B, k, V, eos, crit,
+                            khat, next, status) == cudaSuccess ? VBS_OK : VBS_ECUDA;
 }
 
 template <typename T, bool VECTOR>

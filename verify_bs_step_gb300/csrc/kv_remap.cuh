@@ -8,10 +8,10 @@
 // sentences): the sentence's table rows, reference counts and free stack are
 // loaded into shared memory in one round, new references are counted before old
 // ones are dropped (a block shared by parent and child never reaches zero in
-// between), freed blocks return to the stack in ascending id order, thread 0 makes
-// the block holding position t_valid exclusive to every live row in row order (a
-// fresh block, or a copy-on-write task when it is shared), and the sentence's
-// tasks go to its own slots of the task list.
+// between), freed blocks return to the stack in ascending id order, one warp makes
+// the block holding position t_valid exclusive to every live row (a fresh block, or
+// a copy-on-write task when it is shared; blocks and tasks go to the rows in row
+// order), and the sentence's tasks go to its own slots of the task list.
 #pragma once
 
 #include "common.cuh"
@@ -20,7 +20,7 @@
 namespace vbs {
 
 struct RemapShared {
-  int nold[WMAX], par[WMAX], nnew[WMAX], tail[WMAX], kept[WMAX];
+  int nold[WMAX], par[WMAX], nnew[WMAX], tail[WMAX];
   int top;
 };
 
@@ -114,50 +114,79 @@ __device__ void paged_remap_sentence(const PagedArgs& a, int b, const int32_t* b
   }
   __syncthreads();
   if (tid < 32) {
-    // freed blocks go back on the stack in ascending id order
+    // one warp: freed blocks go back on the stack in ascending id order, then the rows'
+    // tail blocks are decided in parallel (lane w for row w) with the outcome of taking the
+    // rows one after the other in row order
+    const int lane = tid;
+    int top = sh.top;
     for (int j0 = 0; j0 < S; j0 += 32) {
-      const int j = j0 + tid;
+      const int j = j0 + lane;
       const bool freed = j < S && rc0[j] > 0 && rc[j] == 0;
       const u32 m = __ballot_sync(FULL, freed);
-      const int pos = sh.top + __popc(m & ((1u << tid) - 1u));
+      const int pos = top + __popc(m & ((1u << lane) - 1u));
       if (freed && pos < S) stk[pos] = b * S + j;
-      __syncwarp();
-      if (tid == 0) sh.top = min(S, sh.top + __popc(m));
-      __syncwarp();
+      top = min(S, top + __popc(m));
     }
-    // make the block holding position t_valid exclusive to each live row, in row order
-    if (tid == 0) {
-      const int i = t_valid / a.block, fill = t_valid % a.block;
-      int n_kept = 0, n_tasks = 0;
-      for (int w = 0; w < W; ++w) {
-        sh.tail[w] = -1;
-        const int p = sh.par[w];
-        if (p < 0) { sh.nnew[w] = sh.nold[w]; continue; }
+    __syncwarp();
+    // the block holding position t_valid must be exclusive to each live row: a row whose
+    // parent ends just before it takes a fresh block (kind 1); a row whose parent's block
+    // there is shared keeps it if it is the lowest such row, else copies it (kind 2)
+    const int i = t_valid / a.block, fill = t_valid % a.block;
+    const u32 lt = (1u << lane) - 1u;
+    int kind = 0, blk = -1, nnew = 0;
+    if (lane < W) {
+      const int p = sh.par[lane];
+      if (p < 0) {
+        nnew = sh.nold[lane];
+      } else {
         const int n = sh.nold[p - r0];
-        sh.nnew[w] = n;
-        if (n == i) {                                     // a fresh block, nothing to copy
-          if (sh.top == 0) { set_status(a.status, VBS_ENOMEM); continue; }
-          const int nb = stk[--sh.top];
-          rc[nb - b * S] = 1;
-          sh.tail[w] = nb;
-          sh.nnew[w] = i + 1;
+        nnew = n;
+        if (n == i) {
+          kind = 1;
         } else if (n == i + 1) {
-          const int blk = old[(p - r0) * MB + i];
-          if (rc[blk - b * S] == 1) continue;
-          bool is_kept = false;
-          for (int q = 0; q < n_kept; ++q) is_kept |= sh.kept[q] == blk;
-          if (!is_kept) { sh.kept[n_kept++] = blk; continue; }   // the lowest row keeps the shared block
-          if (sh.top == 0) { set_status(a.status, VBS_ENOMEM); continue; }
-          const int nb = stk[--sh.top];
-          rc[nb - b * S] = 1;
-          rc[blk - b * S] -= 1;
-          sh.tail[w] = nb;
-          a.tasks[r0 + n_tasks++] = make_int4(blk, nb, fill, 0);
+          blk = old[(p - r0) * MB + i];
+          if (blk < b * S || blk >= (b + 1) * S) set_status(a.status, VBS_EINVAL);
+          else if (rc[blk - b * S] != 1) kind = 2;
         } else {
           set_status(a.status, VBS_EINVAL);               // the table does not match t_valid
         }
       }
-      for (int q = n_tasks; q < W; ++q) a.tasks[r0 + q] = make_int4(0, 0, 0, 0);
+    }
+    bool keeper = kind == 2;
+    for (int q = 0; q < W; ++q) {                         // a lower row copying the same block
+      const int qk = __shfl_sync(FULL, kind, q), qb = __shfl_sync(FULL, blk, q);
+      if (q < lane && qk == 2 && qb == blk) keeper = false;
+    }
+    if (keeper) kind = 0;
+    // fresh blocks come off the stack in row order; rows past the stack's end get none
+    const u32 need = __ballot_sync(FULL, kind != 0);
+    const int idx = __popc(need & lt);
+    int tail = -1;
+    if (kind != 0) {
+      const int nb = idx < top ? stk[top - 1 - idx] : -1;
+      if (idx < top && (nb < b * S || nb >= (b + 1) * S)) {
+        set_status(a.status, VBS_EINVAL);                 // a corrupt free stack
+        kind = 0;
+      } else if (idx < top) {
+        tail = nb;
+        rc[tail - b * S] = 1;
+        if (kind == 1) nnew = i + 1;
+        else atomicSub(&rc[blk - b * S], 1);
+      } else {
+        set_status(a.status, VBS_ENOMEM);
+        kind = 0;
+      }
+    }
+    const u32 cow = __ballot_sync(FULL, kind == 2);
+    const int n_tasks = __popc(cow);
+    if (kind == 2) a.tasks[r0 + __popc(cow & lt)] = make_int4(blk, tail, fill, 0);
+    if (lane >= n_tasks && lane < W) a.tasks[r0 + lane] = make_int4(0, 0, 0, 0);
+    if (lane < W) {
+      sh.tail[lane] = tail;
+      sh.nnew[lane] = nnew;
+    }
+    if (lane == 0) {
+      sh.top = top - min(__popc(need), top);
       if (n_tasks) atomicAdd(a.cow_slots, static_cast<unsigned long long>(n_tasks) * fill * (a.L * 2 * a.H));
     }
   }
