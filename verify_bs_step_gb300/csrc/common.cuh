@@ -318,4 +318,18 @@ inline bool smem_attr_once(F* fn, int bytes, std::atomic<unsigned long long>& do
   return true;
 }
 
+// Raise a kernel's dynamic shared-memory limit to at least `bytes` on the current device;
+// `set` holds the limit already set per device (a kernel whose need varies by call).
+template <typename F>
+inline bool smem_attr_at_least(F* fn, int bytes, std::atomic<int> (&set)[64]) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  int cur = set[dev].load(std::memory_order_acquire);
+  if (bytes <= cur || bytes <= 48 * 1024) return true;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
+  while (cur < bytes && !set[dev].compare_exchange_weak(cur, bytes, std::memory_order_acq_rel)) {
+  }
+  return true;
+}
+
 }  // namespace vbs

@@ -205,11 +205,8 @@ __global__ void __launch_bounds__(REMAP_NT) kv_paged_remap_kernel(const PagedArg
 int launch_kv_paged_remap(const PagedArgs& a, const int32_t* beam_idx, int t_valid, cudaStream_t s) {
   const size_t smem = static_cast<size_t>(remap_scratch_ints(a)) * sizeof(int32_t);
   if (smem > 200 * 1024) return VBS_EINVAL;
-  static size_t attr = 0;
-  if (smem > 48 * 1024 && smem > attr) {
-    cudaFuncSetAttribute(kv_paged_remap_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    attr = smem;
-  }
+  static std::atomic<int> attr[64];                // the limit set so far, per device
+  if (!smem_attr_at_least(kv_paged_remap_kernel, static_cast<int>(smem), attr)) return VBS_ECUDA;
   return launch_pdl(kv_paged_remap_kernel, dim3(a.B), dim3(REMAP_NT), smem, s, a, beam_idx, t_valid);
 }
 
