@@ -104,6 +104,86 @@ __device__ void warp_select_topk(u64* keys, int n, int K, u64* out, int lane) {
   }
 }
 
+// Descending bitonic sort of 32 keys, one per lane.
+__device__ __forceinline__ u64 warp_sort32(u64 key, int lane) {
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const u64 o = shfl64_xor(key, stride);
+      const bool take_max = ((lane & stride) == 0) == ((lane & size) == 0);   // size 32: all descending
+      key = take_max ? (o > key ? o : key) : (o > key ? key : o);
+    }
+  }
+  return key;
+}
+
+// Two descending 32-key lists held one key per lane (0 = none) to the descending 32 best of
+// their union: lane i's max(a[i], b[31 - i]) are those 32 and form a bitonic sequence, which
+// five compare-exchange stages sort.
+__device__ __forceinline__ u64 warp_merge_top32(u64 a, u64 b, int lane) {
+  const u64 br = shfl64(b, 31 - lane);
+  u64 c = a > br ? a : br;
+#pragma unroll
+  for (int stride = 16; stride > 0; stride >>= 1) {
+    const u64 o = shfl64_xor(c, stride);
+    c = (lane & stride) == 0 ? (o > c ? o : c) : (o > c ? c : o);
+  }
+  return c;
+}
+
+// The K best (K <= 32) of n <= QSEG distinct keys (0 = none), in order, into out[0, K):
+// the K-th best found bit by bit with warp-wide counts, the keys at or above it gathered one
+// per lane and sorted.  out may be overwritten before the end (it holds at most K keys).
+__device__ __forceinline__ void warp_topk_bisect(const u64* keys, int n, int K, u64* out, int lane) {
+  constexpr int PER = QSEG / 32;
+  u64 h[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int j = lane + 32 * i;
+    h[i] = j < n ? keys[j] : 0ull;
+  }
+  u64 x = 0;
+  for (int b = 63; b >= 0; --b) {
+    const u64 c = x | (1ull << b);
+    int cnt = 0;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) cnt += h[i] >= c ? 1 : 0;
+    if (__reduce_add_sync(FULL, static_cast<unsigned>(cnt)) >= static_cast<unsigned>(K)) x = c;
+  }
+  int mine = 0;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) mine += (h[i] != 0ull && h[i] >= x) ? 1 : 0;
+  int pos = mine;                                  // inclusive prefix over the lanes
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int o = __shfl_up_sync(FULL, pos, d);
+    if (lane >= d) pos += o;
+  }
+  const int total = __shfl_sync(FULL, pos, 31);
+  pos -= mine;
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < PER; ++i)
+    if (h[i] != 0ull && h[i] >= x && pos < K) out[pos++] = h[i];
+  __syncwarp();
+  u64 v = lane < min(total, K) ? out[lane] : 0ull;
+  v = warp_sort32(v, lane);
+  __syncwarp();
+  if (lane < K) out[lane] = v;
+  __syncwarp();
+}
+
+// One warp: the K best (K <= 32) of cnt <= 64 distinct keys, in order, into out[0, K): each
+// half sorted, then the 32 best of both.
+__device__ __forceinline__ void warp_sort_top64(const u64* keys, int cnt, int K, u64* out, int lane) {
+  const u64 k0 = lane < cnt ? keys[lane] : 0ull;
+  const u64 k1 = lane + 32 < cnt ? keys[lane + 32] : 0ull;
+  const u64 t = warp_merge_top32(warp_sort32(k0, lane), warp_sort32(k1, lane), lane);
+  __syncwarp();
+  if (lane < K) out[lane] = t;
+}
+
 // K best of nl descending lists of K keys each (keys distinct, 0 = none), in order: K rounds
 // of a warp-wide maximum over the lists' heads; lane c walks lists c, c + 32, ...
 // (nl <= PART_KEYS / 2).
@@ -425,7 +505,7 @@ __device__ void resolve_tiles(const BsArgs& a, SH& sh, int s, int lane) {
 // queued (keys are distinct and QSEG > K, so the bar rises and the passes end).  Only
 // ties at the bar and adversarial orders (e.g. ascending logits) get here.  The aligned
 // path reads 16-byte vectors: the segment may have left L2 by now.
-template <typename T, int VEC>
+template <typename T, int VEC, bool BIGK>
 __device__ void rescan_segment(const BsArgs& a, BsShared& sh, int s) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K = a.K;
@@ -454,7 +534,8 @@ __device__ void rescan_segment(const BsArgs& a, BsShared& sh, int s) {
     named_sync(BAR_CONSUMERS, BS_NC);
     if (sh.qcnt[s] <= QSEG) break;
     if (warp == 0) {
-      warp_select_topk(sh.q[s], QSEG, K, sh.fin[s], lane);
+      if constexpr (BIGK) warp_topk_bisect(sh.q[s], QSEG, K, sh.fin[s], lane);
+      else warp_select_topk(sh.q[s], QSEG, K, sh.fin[s], lane);
       if (lane == 0) sh.rbar[s] = sh.fin[s][K - 1];
     }
   }
@@ -464,6 +545,7 @@ __device__ void rescan_segment(const BsArgs& a, BsShared& sh, int s) {
 
 // One warp: segment s's partial -- (max, scaled sum) over the warps and its K best keys,
 // sorted -- written to its slot of the row's partials; then the slot is cleared.
+template <bool BIGK>
 __device__ void finish_segment(const BsArgs& a, BsShared& sh, int s, int lane) {
   const int K = a.K;
   const int mode = sh.mode[s];
@@ -483,15 +565,20 @@ __device__ void finish_segment(const BsArgs& a, BsShared& sh, int s, int lane) {
     u64* out = a.cluster ? sh.rk[s] : (pslot_ok ? a.part_key + pslot * K : sh.fin[s]);   // cluster mode: in shared memory
     if (mode == 0) {
       const int cnt = sh.fcnt[s];
-      for (int j = lane; j < cnt; j += 32) {
-        const u64 k = sh.fin[s][j];
-        int rank = 0;
-        for (int i = 0; i < cnt; ++i) rank += sh.fin[s][i] > k;
-        if (rank < K) out[rank] = k;
+      if (!BIGK || cnt <= 16) {
+        for (int j = lane; j < cnt; j += 32) {
+          const u64 k = sh.fin[s][j];
+          int rank = 0;
+          for (int i = 0; i < cnt; ++i) rank += sh.fin[s][i] > k;
+          if (rank < K) out[rank] = k;
+        }
+        if (lane < K && lane >= cnt) out[lane] = 0ull;
+      } else if constexpr (BIGK) {
+        warp_sort_top64(sh.fin[s], cnt, K, out, lane);   // up to FIN_CAP = 64 keys
       }
-      if (lane < K && lane >= cnt) out[lane] = 0ull;
     } else {
-      warp_select_topk(sh.q[s], min(sh.qcnt[s], QSEG), K, sh.fin[s], lane);
+      if constexpr (BIGK) warp_topk_bisect(sh.q[s], min(sh.qcnt[s], QSEG), K, sh.fin[s], lane);
+      else warp_select_topk(sh.q[s], min(sh.qcnt[s], QSEG), K, sh.fin[s], lane);
       if (lane < K) out[lane] = sh.fin[s][lane];
     }
     if (lane == 0) {
@@ -519,13 +606,13 @@ __device__ void publish_slots(const BsArgs& a, BsShared& sh, int ns) {
   if (warp < ns) {
     if (!sh.seg_skip[warp]) resolve_tiles<T, VEC, BIGK>(a, sh, warp, lane);
     __syncwarp();
-    if (sh.seg_skip[warp] || sh.mode[warp] != 1) finish_segment(a, sh, warp, lane);
+    if (sh.seg_skip[warp] || sh.mode[warp] != 1) finish_segment<BIGK>(a, sh, warp, lane);
   }
   named_sync(BAR_CONSUMERS, BS_NC);
   for (int s = 0; s < ns; ++s) {
     if (!sh.seg_skip[s] && sh.mode[s] == 1) {      // the same for every thread
-      rescan_segment<T, VEC>(a, sh, s);
-      if (warp == s) finish_segment(a, sh, s, lane);
+      rescan_segment<T, VEC, BIGK>(a, sh, s);
+      if (warp == s) finish_segment<BIGK>(a, sh, s, lane);
     }
   }
 }
@@ -879,7 +966,7 @@ __device__ void cluster_merge_sentence(const BsArgs& a, BsShared& sh, int b, int
     // ---- the sentence's ranking: (score desc, list position asc) = (score desc, flat index asc)
     const int nvalid = __popc(__ballot_sync(FULL, kl != 0ull));
     {
-      const int rank = warp_rank_u32(kl != 0ull ? ord_f32(cl_) : 0u, lane);
+      const int rank = warp_rank_u32(kl != 0ull ? ord_f32(cl_ + 0.0f) : 0u, lane);   // + 0: -0 ranks as +0
       if (kl != 0ull && rank < 2 * W) sh.cm_sel[rank] = lane;
     }
     sh.cm_key[lane] = kl;
@@ -1166,6 +1253,12 @@ __device__ void row_merge(const BsArgs& a, MergeShared& sm, int w, int lane) {
   if (n == 1) {
     if (lane < K) out[lane] = scratch[lane];
     __syncwarp();
+  } else if (8 * (n - 1) < 5 * K) {
+    // few lists of many keys: fold them pairwise, 32 best at a time (lanes >= K hold 0)
+    u64 cur = lane < K ? scratch[lane] : 0ull;
+    for (int j = 1; j < n; ++j) cur = warp_merge_top32(cur, lane < K ? scratch[j * K + lane] : 0ull, lane);
+    if (lane < K) out[lane] = cur;
+    __syncwarp();
   } else {
     warp_merge_sorted(scratch, n, K, out, lane);
   }
@@ -1264,7 +1357,7 @@ __device__ void merge_sentence(const BsArgs& a, MergeShared& sm, int b, int done
       const int w = lane / K, i = lane - w * K;
       const bool valid = lane < W * K && i < sm.nval[w];
       const float c = valid ? sm.candv[lane] : -INFINITY;
-      const int rank = warp_rank_u32(valid ? ord_f32(c) : 0u, lane);
+      const int rank = warp_rank_u32(valid ? ord_f32(c + 0.0f) : 0u, lane);   // + 0: -0 ranks as +0
       if (valid && rank < 2 * W) {
         sm.sel_w[rank] = w;
         sm.sel_i[rank] = i;
@@ -1272,18 +1365,39 @@ __device__ void merge_sentence(const BsArgs& a, MergeShared& sm, int b, int done
       }
     }
   } else if (!was_done) {
-    // rank every candidate of the W lists; the best 2W land in order
-    for (int f = tid; f < W * K; f += NT) {
-      const int w = f / K, i = f - w * K;
-      if (i >= sm.nval[w]) continue;
-      const float c = sm.candv[f];
-      int rank = i;
-      for (int w2 = 0; w2 < W && rank < 2 * W; ++w2)
-        if (w2 != w) rank += count_better(sm.candv + w2 * K, sm.nval[w2], c, w2 < w);
-      if (rank < 2 * W) {
-        sm.sel_w[rank] = w;
-        sm.sel_i[rank] = i;
-        sm.sel_c[rank] = c;
+    // the W lists as keys (score desc, then row and list position asc -- the flat index
+    // order), merged pairwise, 32 best at a time, level by level across the warps (2W <= 32);
+    // the rows' partial lists are consumed, so their scratch holds the levels
+    u64* lev = sm.rowscratch;
+    const auto row_key = [&](int w) -> u64 {
+      if (w >= W || lane >= K || lane >= sm.nval[w]) return 0ull;
+      return (static_cast<u64>(ord_f32(sm.candv[w * K + lane] + 0.0f)) << 32) |   // + 0: -0 ranks as +0
+             static_cast<u64>(~static_cast<u32>((w << 8) | lane));
+    };
+    int m = (W + 1) / 2, src = 0;
+    for (int p = warp; p < m; p += NW) {
+      const u64 r = warp_merge_top32(row_key(2 * p), row_key(2 * p + 1), lane);
+      lev[p * 32 + lane] = r;
+    }
+    cta_sync<NT, BAR>();
+    while (m > 1) {
+      const int m2 = (m + 1) / 2, dst = src ^ 1;
+      for (int p = warp; p < m2; p += NW) {
+        const u64 a0 = lev[src * 512 + (2 * p) * 32 + lane];
+        const u64 b0 = 2 * p + 1 < m ? lev[src * 512 + (2 * p + 1) * 32 + lane] : 0ull;
+        lev[dst * 512 + p * 32 + lane] = warp_merge_top32(a0, b0, lane);
+      }
+      cta_sync<NT, BAR>();
+      m = m2;
+      src = dst;
+    }
+    if (tid < 2 * W) {
+      const u64 k = lev[src * 512 + tid];
+      if (k != 0ull) {
+        const u32 lo = ~static_cast<u32>(k);
+        sm.sel_w[tid] = static_cast<int>(lo >> 8);
+        sm.sel_i[tid] = static_cast<int>(lo & 0xffu);
+        sm.sel_c[tid] = unord_f32(static_cast<u32>(k >> 32));
       }
     }
   }
