@@ -320,8 +320,9 @@ __device__ __forceinline__ u32 warp_kth_u32(u32 v, int K, int lane) {
   return __shfl_sync(FULL, v, __ffs(b) - 1);
 }
 
-// warp_kth_u32 out of line, for the streaming loop's once-per-row seed: the hot loop's code
-// stays smaller for the instruction caches (measured 3 % faster at the Llama shape).
+// warp_kth_u32 out of line, for the K <= 8 streaming loop's once-per-row seed: the hot loop's
+// code stays smaller for the instruction caches (measured 3 % faster at the Llama shape; the
+// K > 8 instance measured slower with it and keeps the seed inline).
 __device__ __noinline__ u32 warp_kth_u32_cold(u32 v, int K, int lane) { return warp_kth_u32(v, K, lane); }
 
 // Warp-wide: the K-th best of the lane maxima of the first n entries' tile maxima (0 if
@@ -621,9 +622,9 @@ __device__ void publish_slots(const BsArgs& a, BsShared& sh, int ns) {
   }
 }
 
-// publish_slots out of line, for the streaming loop's publish when every slot holds a segment
-// (the stream kernel's long ranges): inlined, its resolve, finish and rescan code enlarged the
-// loop's code (3 % slower at the Llama shape, where it never runs).
+// publish_slots out of line, for the K <= 8 streaming loop's publish when every slot holds a
+// segment (the stream kernel's long ranges): inlined, its resolve, finish and rescan code
+// enlarged the loop's code (3 % slower at the Llama shape, where it never runs).
 template <typename T, int VEC, bool BIGK>
 __device__ __noinline__ void publish_slots_cold(const BsArgs& a, BsShared& sh, int ns) {
   publish_slots<T, VEC, BIGK>(a, sh, ns);
@@ -643,6 +644,8 @@ __device__ void consume(const BsArgs& a, BsShared& sh, int64_t e0, int64_t e1) {
   float M = -INFINITY, m = -INFINITY, l = 0.f;
   bool skip = false, seeded = false;
   int seg = -1, slot = 0;
+  int rs = 0;                                       // ring stage of chunk c, and its phase
+  u32 ph = 0;
   ChunkCursor cur(e0, e1, a.V, static_cast<int>(SE));
   for (int c = 0; cur.more(); ++c) {
     const Chunk ch = cur.next();
@@ -651,7 +654,8 @@ __device__ void consume(const BsArgs& a, BsShared& sh, int64_t e0, int64_t e1) {
       slot = seg % NSLOT;
       if (seg > 0 && slot == 0) {                   // every slot holds a segment: publish them
         named_sync(BAR_CONSUMERS, BS_NC);
-        publish_slots_cold<T, VEC, BIGK>(a, sh, NSLOT);
+        if constexpr (BIGK) publish_slots<T, VEC, BIGK>(a, sh, NSLOT);   // K > 8: frequent, kept inline
+        else publish_slots_cold<T, VEC, BIGK>(a, sh, NSLOT);
         named_sync(BAR_CONSUMERS, BS_NC);
       }
       if constexpr (!TMA) skip = row_skipped(a, ch.r);
@@ -664,17 +668,23 @@ __device__ void consume(const BsArgs& a, BsShared& sh, int64_t e0, int64_t e1) {
     uint4 q[BS_U];
     float xs[BS_U];
     if constexpr (TMA) {
-      const int rs = c % NSTAGE;
-      if (!mbar_wait(&sh.full[rs], static_cast<u32>((c / NSTAGE) & 1))) set_status(a.status, VBS_ETIMEOUT);
+      if (!mbar_wait(&sh.full[rs], ph)) set_status(a.status, VBS_ETIMEOUT);
       skip = sh.stage_skip[rs] != 0;                // the producer's decision for this row
+      const uint4* stage = reinterpret_cast<const uint4*>(sh.ring[rs]) + tid;
+      if (!skip && n == BS_NC * BS_U) {             // a full chunk: no per-vector bounds
 #pragma unroll
-      for (int u = 0; u < BS_U; ++u) {
-        const int i = tid + u * BS_NC;
-        constexpr u32 NEG = VecMax<T>::NEG;
-        q[u] = (!skip && i < n) ? *reinterpret_cast<const uint4*>(sh.ring[rs] + i * 16) : make_uint4(NEG, NEG, NEG, NEG);
+        for (int u = 0; u < BS_U; ++u) q[u] = stage[u * BS_NC];
+      } else {
+#pragma unroll
+        for (int u = 0; u < BS_U; ++u) {
+          const int i = tid + u * BS_NC;
+          constexpr u32 NEG = VecMax<T>::NEG;
+          q[u] = (!skip && i < n) ? stage[u * BS_NC] : make_uint4(NEG, NEG, NEG, NEG);
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.empty[rs]);    // the stage may refill once every warp has its data
+      if (++rs == NSTAGE) { rs = 0; ph ^= 1u; }
     } else {
       const char* row = reinterpret_cast<const char*>(a.logits) +
                         (static_cast<int64_t>(ch.r) * a.ld + ch.v0) * Elem<T>::BYTES;
@@ -710,13 +720,13 @@ __device__ void consume(const BsArgs& a, BsShared& sh, int64_t e0, int64_t e1) {
         // every consumer warp is at the segment's first chunk: the threshold starts at
         // the best of the warps' seeds, so only a few tiles of this chunk are queued
         seeded = true;
-        const u32 seed = warp_kth_u32_cold(tmo, K, lane);
+        const u32 seed = BIGK ? warp_kth_u32(tmo, K, lane) : warp_kth_u32_cold(tmo, K, lane);
         if (lane == 0 && seed > thr_o) atomicMax(&sh.thr[slot], seed);
         if constexpr (BIGK) {
           // a second bound: each of the BS_NCW warps has j = ceil(K / BS_NCW) lane maxima
           // at or above its own j-th best, so at least K tiles reach the least of those
           // (with K > 8 the warps' K-th bests alone let most of the chunk's tiles in)
-          const u32 seed_j = warp_kth_u32_cold(tmo, (K + BS_NCW - 1) / BS_NCW, lane);
+          const u32 seed_j = warp_kth_u32(tmo, (K + BS_NCW - 1) / BS_NCW, lane);
           if (lane == 0) atomicMin(&sh.tmin[slot], seed_j);
         }
         named_sync(BAR_CONSUMERS, BS_NC);
