@@ -429,7 +429,10 @@ int bpd_propose(const void* logits, int B, int k, int V, int dtype, int32_t* pro
  * ready list (4 MiB) are static device memory shared by every call (reset by
  * each call's last CTA): two bpd_verify calls that overlap on the GPU
  * (different streams or host threads) race and must be serialised by the
- * caller.  A wait that gives up is reported by vbs_stateless_status().
+ * caller.  Calls on one stream are ordered: the kernel is launched as a
+ * programmatic dependent, so its set-up may overlap the previous kernel, but it
+ * touches memory only once that kernel has completed.  A wait that gives up is
+ * reported by vbs_stateless_status().
  * Errors: VBS_EINVAL (B < 0, k outside 1..32, V < 1, eos >= V, unknown dtype,
  *   NULL pointers with B > 0), VBS_ECUDA.
  */
