@@ -32,9 +32,12 @@
  *   - Logits are row-major with a row stride `ld` (elements) >= V; dtype is
  *     VBS_F32 or VBS_BF16.  Logits must be finite or -inf, with at least one
  *     finite value per row that is read.
- *   - One device per process: the kernels' shared-memory attributes are set
- *     once per process, on the device current at the first launch.  A process
- *     that drives several GPUs runs one process per GPU (as the bench does).
+ *   - Devices: every call works on the device current on the calling thread,
+ *     and the stream it is given must belong to that device.  The kernels'
+ *     shared-memory attributes are set once per device, and the library's
+ *     static device memory (bs_expand_static's scratch, bpd_verify's queue,
+ *     the status word of the calls without a context) exists once per device.
+ *     The bench runs one process per GPU.
  */
 #ifndef VBS_H
 #define VBS_H
