@@ -969,6 +969,15 @@ def run_profile(kernel: str):
             else:
                 bs.step_two_pass(ring[i % 3])
         bs.close()
+    elif kernel == "bs_step_w16":
+        # the wide-beam sweep shape 256 x 16 x 32000 bf16 (two-kernel path, K = 32)
+        B, W, V = 256, 16, 32000
+        ring = [synth.batch_logits("sweep", B, W, V, seed=2024 + i, step=i, eos=7, dtype=torch.bfloat16, device=dev)
+                for i in range(3)]
+        bs = vbs.BeamSearch(B, W, V, eos=7, alpha=0.6, max_len=50, dtype=torch.bfloat16, device=dev)
+        for i in range(6):
+            bs.step(ring[i % 3])
+        bs.close()
     elif kernel == "bpd_verify":
         B, k, V = 256, 8, 32000
         base, props, heads = synth.geometric_prefix_proposals(B, k, V, seed=500, step=0)
